@@ -1,0 +1,214 @@
+"""CPU oracle for the block-sparse attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Loads ``bsattn_oracle.c`` (plain C, fp64; compiled here with gcc) through
+ctypes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA library,
+and nothing in the product path imports it.
+
+Functions follow the varlen block-sparsity pull request (flash-attention
+#2224, description and review) for the metadata layout and the block-sparse
+learning note ("Dense FlashAttention vs Block-Sparse Attention", section 2) for
+the reversed, -1-padded index lists; the C file's header lists each source and
+every reading taken where the pages leave a step open.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsattn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.POINTER(ctypes.c_int32)
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("varlen", ctypes.c_int32), ("num_m", ctypes.c_int32), ("num_n", ctypes.c_int32),
+                ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("cu_q", _P), ("cu_k", _P), ("kv_valid_len", _P), ("vl_stride", ctypes.c_int32),
+                ("kind", ctypes.c_int32), ("window_left", ctypes.c_int32),
+                ("sink_tokens", ctypes.c_int32), ("prefix_len", ctypes.c_int32),
+                ("doc_q", _P), ("doc_k", _P)]
+
+
+class Meta(ctypes.Structure):
+    _fields_ = [("full_cnt", _P), ("full_idx", _P), ("mask_cnt", _P), ("mask_idx", _P),
+                ("cu_total_m_blocks", _P), ("cu_block_idx_offsets", _P),
+                ("total_m_blocks", ctypes.c_int32), ("total_n_blocks", ctypes.c_int32)]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into liboracle.so next to its source."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = f"{_LIB}.tmp.{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+                    "-lm", "-lpthread"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load(path=None):
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            if path is None:
+                build()
+            lib = ctypes.CDLL(path or _LIB)
+            lib.oracle_varlen_offsets.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(Meta)]
+            lib.oracle_varlen_offsets.restype = ctypes.c_int
+            lib.oracle_build_meta.argtypes = [ctypes.POINTER(Problem), ctypes.c_void_p,
+                                              ctypes.POINTER(Meta), ctypes.c_int]
+            lib.oracle_build_meta.restype = ctypes.c_int
+            lib.oracle_fwd_rows.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(Meta),
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_double, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_int]
+            lib.oracle_fwd_rows.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _use_library(path=None):
+    """Point this module at another compiled copy of the oracle (the mutation
+    tests use it to check that planted mistakes are caught); None restores the
+    library built from bsattn_oracle.c."""
+    global _lib
+    if path is None:
+        with _lock:
+            _lib = None
+        _load()
+    else:
+        _load(path)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_P)
+
+
+class _Holder:
+    """Keeps the numpy arrays behind a Problem alive while C uses them."""
+
+    def __init__(self, wl):
+        self.cu_q = np.ascontiguousarray(wl.cu_seqlens_q, dtype=np.int32)
+        self.cu_k = np.ascontiguousarray(wl.cu_seqlens_k, dtype=np.int32)
+        self.vl = (None if wl.kv_valid_len is None
+                   else np.ascontiguousarray(wl.kv_valid_len, dtype=np.int32))
+        self.dq = None if wl.doc_id_q is None else np.ascontiguousarray(wl.doc_id_q, np.int32)
+        self.dk = None if wl.doc_id_k is None else np.ascontiguousarray(wl.doc_id_k, np.int32)
+        self.p = Problem(B=wl.B, H=wl.H, D=wl.D, varlen=int(wl.varlen), num_m=wl.num_m,
+                         num_n=wl.num_n, tile_m=wl.tile_m, tile_n=wl.tile_n,
+                         cu_q=_ptr(self.cu_q), cu_k=_ptr(self.cu_k), kv_valid_len=_ptr(self.vl),
+                         vl_stride=(0 if self.vl is None else self.vl.shape[-1]),
+                         kind=wl.kind, window_left=wl.window_left, sink_tokens=wl.sink_tokens,
+                         prefix_len=wl.prefix_len, doc_q=_ptr(self.dq), doc_k=_ptr(self.dk))
+
+
+def meta_shapes(wl):
+    """Shapes of (cnt, idx) arrays: batched [B,H,num_m] / [B,H,num_m,num_n];
+    varlen [H,total_m_blocks] / [H,total_n_blocks]."""
+    if wl.varlen:
+        return (wl.H, wl.total_m_blocks), (wl.H, wl.total_n_blocks)
+    return (wl.B, wl.H, wl.num_m), (wl.B, wl.H, wl.num_m, wl.num_n)
+
+
+def build_meta(wl, block_map=None, threads=None) -> dict:
+    """Metadata lists for workload `wl` (its own block map unless one is given)."""
+    lib = _load()
+    hold = _Holder(wl)
+    bm = np.ascontiguousarray(wl.block_map if block_map is None else block_map, dtype=np.uint8)
+    cs, is_ = meta_shapes(wl)
+    out = {"full_cnt": np.empty(cs, np.int32), "full_idx": np.empty(is_, np.int32),
+           "mask_cnt": np.empty(cs, np.int32), "mask_idx": np.empty(is_, np.int32),
+           "cu_total_m_blocks": np.zeros(wl.B + 1, np.int32),
+           "cu_block_idx_offsets": np.zeros(wl.B + 1, np.int32)}
+    mt = Meta(full_cnt=_ptr(out["full_cnt"]), full_idx=_ptr(out["full_idx"]),
+              mask_cnt=_ptr(out["mask_cnt"]), mask_idx=_ptr(out["mask_idx"]),
+              cu_total_m_blocks=_ptr(out["cu_total_m_blocks"]),
+              cu_block_idx_offsets=_ptr(out["cu_block_idx_offsets"]),
+              total_m_blocks=0, total_n_blocks=0)
+    rc = lib.oracle_build_meta(ctypes.byref(hold.p), bm.ctypes.data, ctypes.byref(mt),
+                               threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_build_meta rejected the problem")
+    if wl.varlen:
+        out["total_m_blocks"], out["total_n_blocks"] = mt.total_m_blocks, mt.total_n_blocks
+    return out
+
+
+def varlen_offsets(wl):
+    """(cu_total_m_blocks, cu_block_idx_offsets) for a varlen workload."""
+    lib = _load()
+    hold = _Holder(wl)
+    cm = np.zeros(wl.B + 1, np.int32)
+    cn = np.zeros(wl.B + 1, np.int32)
+    mt = Meta(cu_total_m_blocks=_ptr(cm), cu_block_idx_offsets=_ptr(cn))
+    if lib.oracle_varlen_offsets(ctypes.byref(hold.p), ctypes.byref(mt)) != 0:
+        raise ValueError("bad sequence lengths")
+    return cm, cn
+
+
+def fwd_rows(wl, q, k, v, meta, tok, head, threads=None):
+    """O (fp64 [n, D]) and LSE (fp64 [n]) for packed query rows `tok`, heads `head`.
+
+    q/k/v are raw bf16 bits (uint16) in the workload's layout; `meta` is a dict
+    as returned by build_meta (lists of this oracle, never of the CUDA path)."""
+    lib = _load()
+    hold = _Holder(wl)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    head = np.ascontiguousarray(head, dtype=np.int32)
+    n = tok.size
+    o = np.empty((n, wl.D), np.float64)
+    lse = np.empty(n, np.float64)
+    arrs = {key: np.ascontiguousarray(meta[key], dtype=np.int32)
+            for key in ("full_cnt", "full_idx", "mask_cnt", "mask_idx",
+                        "cu_total_m_blocks", "cu_block_idx_offsets")}
+    mt = Meta(full_cnt=_ptr(arrs["full_cnt"]), full_idx=_ptr(arrs["full_idx"]),
+              mask_cnt=_ptr(arrs["mask_cnt"]), mask_idx=_ptr(arrs["mask_idx"]),
+              cu_total_m_blocks=_ptr(arrs["cu_total_m_blocks"]),
+              cu_block_idx_offsets=_ptr(arrs["cu_block_idx_offsets"]),
+              total_m_blocks=int(meta.get("total_m_blocks", 0)),
+              total_n_blocks=int(meta.get("total_n_blocks", 0)))
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    rc = lib.oracle_fwd_rows(ctypes.byref(hold.p), ctypes.byref(mt), q.ctypes.data,
+                             k.ctypes.data, v.ctypes.data, float(wl.scale), n,
+                             tok.ctypes.data, head.ctypes.data, o.ctypes.data, lse.ctypes.data,
+                             threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_fwd_rows rejected a row")
+    return o, lse
+
+
+def fwd(wl, q, k, v, meta, threads=None):
+    """Every query row of every head.
+
+    Returns O as fp64 in q's layout and LSE as fp64 in the library's layout:
+    batched [B, H, S_q], varlen [H, total_q]."""
+    rows = wl.rows_q
+    tok = np.tile(np.arange(rows, dtype=np.int32), wl.H)
+    head = np.repeat(np.arange(wl.H, dtype=np.int32), rows)
+    o, lse = fwd_rows(wl, q, k, v, meta, tok, head, threads)
+    o = o.reshape(wl.H, rows, wl.D).transpose(1, 0, 2)           # [rows, H, D]
+    lse = lse.reshape(wl.H, rows)                                  # [H, rows]
+    if wl.varlen:
+        return np.ascontiguousarray(o), np.ascontiguousarray(lse)
+    S = int(wl.seqlens_q[0])
+    o = o.reshape(wl.B, S, wl.H, wl.D)
+    lse = lse.reshape(wl.H, wl.B, S).transpose(1, 0, 2)            # [B, H, S]
+    return np.ascontiguousarray(o), np.ascontiguousarray(lse)
