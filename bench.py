@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse attention forward on GB300.
+
+One step = the whole hot path over one batch of synthetic input: the metadata
+kernel (boolean block map -> full / mask lists) and the attention kernel.
+Default workload: video sparse attention, B=1 H=24 S=61440 d=128, top-32 of 240
+logical 256-token KV blocks per logical Q block, valid length U[192,256] per
+logical block, run as 128-token tiles (737,280 computed tiles, 6.185 TFLOP).
+
+Metric: effective TFLOP/s = sum over computed tiles of 4 * 128 * 128 * d,
+divided by the time.  Also reported: the attention kernel's own roofline
+(CUDA events around its launches), an end-to-end number through the public
+API with pinned host buffers (host->device inputs and device->host outputs
+inside the timed region), and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Under torchrun each rank runs its own replica on its own GPU (no data-path
+collective); rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s over computed blocks, bf16 fwd; % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_CONFIG = 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG,
+                    help="workload number (1-5); the benchmark line uses 4")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def flop_per_tile(d: int) -> int:
+    return 4 * 128 * 128 * d
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_index is not None:
+            cmd += ["-i", str(gpu_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for name, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_index_for_smi(torch, dev):
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", None)
+        devid = getattr(props, "pci_device_id", None)
+        if bus is not None and dom is not None and devid is not None:
+            return f"{dom:08x}:{bus:02x}:{devid:02x}.0"
+    except Exception:
+        pass
+    return None
+
+
+def one_head(wl, q, k, v):
+    """Head 0 of a workload as a workload of its own (heads are independent)."""
+    import numpy as np
+    from dataclasses import replace
+    bm = wl.block_map[:1] if wl.varlen else wl.block_map[:, :1]
+    w1 = replace(wl, H=1, block_map=np.ascontiguousarray(bm))
+    cut = (lambda x: np.ascontiguousarray(x[:, :1])) if wl.varlen else (
+        lambda x: np.ascontiguousarray(x[:, :, :1]))
+    return w1, cut(q), cut(k), cut(v)
+
+
+def cpu_baseline(wl, q, k, v, seconds, threads=None):
+    """The oracle on whole Q tiles of head 0, drawn at random, until about
+    `seconds` of oracle time; returns (TFLOP/s over the sample's computed tiles,
+    threads used, description of the sample)."""
+    import numpy as np
+    import oracle
+    threads = threads or oracle.default_threads()
+    w1, q1, k1, v1 = one_head(wl, q, k, v)
+    meta = oracle.build_meta(w1, threads=threads)
+    cnt = (meta["full_cnt"] + meta["mask_cnt"]).reshape(-1)     # per packed Q tile
+    starts = (np.concatenate([[0], np.cumsum(np.ceil(w1.seqlens_q / 128).astype(int))])
+              if w1.varlen else None)
+    rng = np.random.default_rng(0)
+    done_flop, done_tiles, elapsed = 0, 0, 0.0
+    while elapsed < seconds and done_tiles < 4096:
+        t = int(rng.integers(0, cnt.size))
+        if w1.varlen:
+            b = int(np.searchsorted(starts, t, side="right") - 1)
+            r0 = int(w1.cu_seqlens_q[b]) + (t - int(starts[b])) * 128
+            r1 = min(r0 + 128, int(w1.cu_seqlens_q[b + 1]))
+        else:
+            S = int(w1.seqlens_q[0])
+            b, m = divmod(t, S // 128 if S % 128 == 0 else -(-S // 128))
+            r0 = b * S + m * 128
+            r1 = min(r0 + 128, (b + 1) * S)
+        tok = np.arange(r0, r1, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.fwd_rows(w1, q1, k1, v1, meta, tok, np.zeros_like(tok), threads=threads)
+        elapsed += time.perf_counter() - t0
+        done_flop += int(cnt[t]) * flop_per_tile(wl.D)
+        done_tiles += 1
+    value = done_flop / elapsed / 1e12
+    desc = (f"oracle (fp64, plain C, {threads} threads) on {done_tiles} whole Q tiles of head 0 "
+            f"drawn at random from the workload: {done_flop / 1e9:.1f} GFLOP of computed tiles "
+            f"in {elapsed:.1f} s")
+    return value, threads, desc
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from workloads import make_workload
+    wl = make_workload(args.config)
+    q, k, v = wl.qkv()
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, q, k, v, per_step)
+    vals = []
+    t0 = time.perf_counter()
+    threads = oracle.default_threads()
+    desc = ""
+    for _ in range(args.steps):
+        val, threads, desc = cpu_baseline(wl, q, k, v, per_step)
+        vals.append(val)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "S": int(wl.seqlens_q[0]),
+                       "D": wl.D},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+
+    import block_sparse_flashattention_gb300 as bsa
+    from tests.gpu_run import DeviceWorkload, meta_to_numpy, computed_blocks
+    from workloads import make_workload
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    wl = make_workload(args.config)
+    # inputs in pinned host memory (the e2e leg copies them every step)
+    pin = dict(pin_memory=True)
+    hq = torch.empty(wl.q_shape(), dtype=torch.int16, **pin)
+    hk = torch.empty(wl.k_shape(), dtype=torch.int16, **pin)
+    hv = torch.empty(wl.k_shape(), dtype=torch.int16, **pin)
+    wl.fill("q", hq.data_ptr())
+    wl.fill("k", hk.data_ptr())
+    wl.fill("v", hv.data_ptr())
+    hmap = torch.from_numpy(np.ascontiguousarray(wl.block_map)).pin_memory()
+    hvl = (torch.from_numpy(np.ascontiguousarray(wl.kv_valid_len)).pin_memory()
+           if wl.kv_valid_len is not None else None)
+
+    dw = DeviceWorkload(wl, dev, qkv=False)
+    dw.q = hq.to(dev).view(torch.bfloat16)
+    dw.k = hk.to(dev).view(torch.bfloat16)
+    dw.v = hv.to(dev).view(torch.bfloat16)
+    meta = dw.alloc_meta()
+    out = torch.empty_like(dw.q)
+    sq, sk = dw.seqlens()
+    lse = torch.empty((wl.H, wl.rows_q) if wl.varlen else (wl.B, wl.H, sq), dtype=torch.float32,
+                      device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dw.build_meta(meta, err_flag=err)
+        dw.forward(meta, out=out, lse=lse, err_flag=err)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())}")
+    blocks = computed_blocks(meta_to_numpy(meta))
+    flop_step = blocks * flop_per_tile(wl.D)
+
+    # ---------------------------------------------------------- timed region
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_index_for_smi(torch, dev))
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        dw.build_meta(meta, err_flag=err)
+        ev[i][1].record(stream)
+        dw.forward(meta, out=out, lse=lse, err_flag=err)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    meta_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    fwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = ws * flop_step * K / (total_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------- end-to-end leg
+    h_out = torch.empty(out.shape, dtype=torch.int16, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+    d_map = dw.block_map
+    d_vl = dw.vl
+
+    def e2e_step():
+        dw.q.view(torch.int16).copy_(hq, non_blocking=True)
+        dw.k.view(torch.int16).copy_(hk, non_blocking=True)
+        dw.v.view(torch.int16).copy_(hv, non_blocking=True)
+        d_map.copy_(hmap, non_blocking=True)
+        if d_vl is not None:
+            d_vl.copy_(hvl, non_blocking=True)
+        step()
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + hmap.numel() + (
+        hvl.numel() * 4 if hvl is not None else 0)
+    d2h = out.numel() * 2 + lse.numel() * 4
+    e2e_value = ws * flop_step * K / (e2e_ms * 1e-3) / 1e12
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())}")
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    fwd_mean = statistics.mean(fwd_ms)
+    achieved = flop_step / (fwd_mean * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "bsattn_fwd_traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tr = json.load(f)
+            if tr.get("workload") == wl.name:
+                traffic = tr.get("bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        q_np = hq.numpy().view(np.uint16)
+        k_np = hk.numpy().view(np.uint16)
+        v_np = hv.numpy().view(np.uint16)
+        cval, cores, desc = cpu_baseline(wl, q_np, k_np, v_np, args.cpu_seconds)
+        cpu = {"value": cval, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "S": sq, "D": wl.D,
+                   "tile": "128x128", "computed_tiles": blocks,
+                   "flop_per_step": flop_step,
+                   "step": "metadata kernel + attention kernel",
+                   "l2": "inputs larger than L2 (Q/K/V %.2f GB vs 129 MB)" % (
+                       3 * hq.numel() * 2 / 1e9),
+                   "parallelism": f"replicas x{ws}"},
+        "fwd_ms": fwd_mean, "meta_ms": statistics.mean(meta_ms),
+        "fwd_tflops": achieved, "frac_of_peak_step": value / ws / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
+                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained",
+                                                                      peak))},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
+        "gpu_launches": K * (2 + (1 if wl.varlen else 0)),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

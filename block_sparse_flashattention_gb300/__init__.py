@@ -1,0 +1,103 @@
+"""Block-sparse attention forward for NVIDIA GB300 (sm_103a).
+
+The compute path is the CUDA library libbsattn.so (include/bsattn.h): a metadata
+kernel that turns a boolean block map into full / mask block lists, and a
+persistent TMA + tcgen05 attention kernel that walks those lists.  This package
+is the Python face of that C ABI: ``bsattn_build_meta`` and ``bsattn_fwd`` carry
+the C names and only marshal arguments; ``alloc_meta``, ``build_meta`` and
+``forward`` add torch allocation of the outputs around them.  PyTorch provides
+device memory and streams only.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+from ._binding import (BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUPPORTED,
+                       BSATTN_OK, FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_BAD_SEQLENS, FLAG_TIMEOUT,
+                       MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX, MASK_SLIDING_WINDOW,
+                       BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
+                       bsattn_fwd, library, status_string)
+
+TILE = 128
+
+__all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_abi_version", "alloc_meta", "build_meta",
+           "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
+           "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
+           "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA",
+           "FLAG_BAD_COUNT", "FLAG_BAD_INDEX", "FLAG_TIMEOUT", "FLAG_BAD_SEQLENS"]
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def alloc_meta(B: int, H: int, *, varlen: bool = False, seqlen_q: int = 0, seqlen_k: int = 0,
+               total_m_blocks: int = 0, total_n_blocks: int = 0, max_num_n: int = 0,
+               device="cuda") -> Meta:
+    """Allocates the metadata tensors.
+
+    Batched: pass seqlen_q / seqlen_k (per sequence).  Varlen: pass
+    total_m_blocks, total_n_blocks (sum of num_m(b) and of num_m(b) * num_n(b))
+    and max_num_n (row stride of kv_valid_len, at least the largest num_n(b))."""
+    import torch
+    i32 = dict(dtype=torch.int32, device=device)
+    if varlen:
+        return Meta(full_cnt=torch.empty((H, total_m_blocks), **i32),
+                    full_idx=torch.empty((H, total_n_blocks), **i32),
+                    mask_cnt=torch.empty((H, total_m_blocks), **i32),
+                    mask_idx=torch.empty((H, total_n_blocks), **i32), varlen=1, B=B, H=H,
+                    num_m=0, num_n=max_num_n, total_m_blocks=total_m_blocks,
+                    total_n_blocks=total_n_blocks,
+                    cu_total_m_blocks=torch.empty(B + 1, **i32),
+                    cu_block_idx_offsets=torch.empty(B + 1, **i32))
+    nm, nn = _cdiv(seqlen_q, TILE), _cdiv(seqlen_k, TILE)
+    return Meta(full_cnt=torch.empty((B, H, nm), **i32),
+                full_idx=torch.empty((B, H, nm, nn), **i32),
+                mask_cnt=torch.empty((B, H, nm), **i32),
+                mask_idx=torch.empty((B, H, nm, nn), **i32), varlen=0, B=B, H=H, num_m=nm,
+                num_n=nn)
+
+
+def _check(status: int, where: str) -> None:
+    if status != BSATTN_OK:
+        raise BsattnError(status, where)
+
+
+def build_meta(block_map, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, seqlen_q: int = 0,
+               seqlen_k: int = 0, kv_valid_len=None, kind: int = MASK_NONE,
+               mask_params: Optional[MaskParams] = None, err_flag=None, stream=None) -> Meta:
+    """Runs the metadata kernel into `meta` (see alloc_meta); raises on a bad status."""
+    _check(bsattn_build_meta(block_map, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k,
+                             kv_valid_len, kind, mask_params, meta, err_flag, stream),
+           "bsattn_build_meta")
+    return meta
+
+
+def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_valid_len=None,
+            kind: int = MASK_NONE, mask_params: Optional[MaskParams] = None,
+            softmax_scale: Optional[float] = None, out=None, lse=None, err_flag=None,
+            stream=None):
+    """Block-sparse attention forward.  q/k/v: bf16 [B, S, H, D] or packed [total, H, D].
+
+    Returns (out, lse): out like q, lse fp32 [B, H, S_q] (batched) or [H, total_q]."""
+    import torch
+    varlen = bool(meta.varlen)
+    if varlen:
+        rows_q, H, D = q.shape
+        seqlen_q, seqlen_k = rows_q, k.shape[0]
+        lse_shape = (H, rows_q)
+    else:
+        _, seqlen_q, H, D = q.shape
+        seqlen_k = k.shape[1]
+        lse_shape = (meta.B, H, seqlen_q)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    _check(bsattn_fwd(q, k, v, meta.B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta,
+                      kv_valid_len, kind, mask_params, softmax_scale, out, lse, err_flag, stream),
+           "bsattn_fwd")
+    return out, lse

@@ -1,0 +1,251 @@
+// C-ABI entry points: host-side validation, TMA tensor maps, kernel launches.
+// Nothing here allocates device memory or synchronises with the device.
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "bsattn_internal.h"
+
+namespace {
+
+using bsattn::kTile;
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bsattn_status check_mask(bsattn_mask_kind kind, const bsattn_mask_params *mp) {
+    switch (kind) {
+    case BSATTN_MASK_NONE:
+    case BSATTN_MASK_CAUSAL:
+        return BSATTN_OK;
+    case BSATTN_MASK_SLIDING_WINDOW:
+        if (!mp || mp->window_left < 0 || mp->sink_tokens < 0) return BSATTN_ERR_INVALID_ARG;
+        return BSATTN_OK;
+    case BSATTN_MASK_PREFIX:
+        if (!mp || mp->prefix_len < 0) return BSATTN_ERR_INVALID_ARG;
+        return BSATTN_OK;
+    case BSATTN_MASK_DOCUMENT:
+        if (!mp || !mp->doc_id_q || !mp->doc_id_k) return BSATTN_ERR_INVALID_ARG;
+        return BSATTN_OK;
+    default:
+        return BSATTN_ERR_INVALID_ARG;
+    }
+}
+
+// Common checks on the metadata descriptor.
+bsattn_status check_meta(const bsattn_meta *m) {
+    if (!m) return BSATTN_ERR_INVALID_ARG;
+    if (m->tile_m != kTile || m->tile_n != kTile) return BSATTN_ERR_UNSUPPORTED;
+    if (m->B <= 0 || m->H <= 0) return BSATTN_ERR_INVALID_ARG;
+    if (!m->full_cnt || !m->full_idx || !m->mask_cnt || !m->mask_idx) return BSATTN_ERR_INVALID_ARG;
+    if (m->varlen != 0 && m->varlen != 1) return BSATTN_ERR_INVALID_ARG;
+    if (m->varlen) {
+        if (!m->cu_total_m_blocks || !m->cu_block_idx_offsets) return BSATTN_ERR_INVALID_ARG;
+        if (m->total_m_blocks < 0 || m->total_n_blocks < 0 || m->num_n < 0)
+            return BSATTN_ERR_INVALID_ARG;
+    } else {
+        if (m->num_m < 0 || m->num_n < 0) return BSATTN_ERR_INVALID_ARG;
+        if ((long long)m->B * m->H * m->num_m > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+    }
+    return BSATTN_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [rows, H, D] bf16 tensor; box = 128 rows x 1 head x 64 columns, 128-byte swizzle.
+bool encode_bshd(CUtensorMap *map, const void *ptr, long long rows, int H, int D) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bsattn_status_string(bsattn_status s) {
+    switch (s) {
+    case BSATTN_OK: return "BSATTN_OK";
+    case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
+    case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
+    case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
+    default: return "BSATTN_ERR_UNKNOWN";
+    }
+}
+
+int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
+
+bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
+                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
+                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                int32_t *err_flag, void *stream) {
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
+    if (!block_map) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.map = block_map;
+    p.varlen = meta->varlen;
+    p.B = meta->B;
+    p.H = meta->H;
+    p.num_m = meta->num_m;
+    p.num_n = meta->num_n;
+    if (meta->varlen) {
+        if (!cu_seqlens_q || !cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
+        if (kv_valid_len && meta->num_n <= 0) return BSATTN_ERR_INVALID_ARG;
+        p.total_m = meta->total_m_blocks;
+        p.total_n = meta->total_n_blocks;
+        if ((long long)p.H * p.total_m > INT32_MAX * 8LL) return BSATTN_ERR_INVALID_ARG;
+    } else {
+        if (cu_seqlens_q || cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
+        if (seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
+        if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+            return BSATTN_ERR_INVALID_ARG;
+        if ((long long)meta->B * seqlen_q > INT32_MAX || (long long)meta->B * seqlen_k > INT32_MAX)
+            return BSATTN_ERR_INVALID_ARG;
+    }
+    p.seqlen_q = seqlen_q;
+    p.seqlen_k = seqlen_k;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.cu_tm = meta->cu_total_m_blocks;
+    p.cu_off = meta->cu_block_idx_offsets;
+    p.vl = kv_valid_len;
+    p.vl_stride = meta->num_n;
+    p.kind = (int)kind;
+    if (mp) {
+        p.window_left = mp->window_left;
+        p.sink_tokens = mp->sink_tokens;
+        p.prefix_len = mp->prefix_len;
+        p.doc_q = mp->doc_id_q;
+        p.doc_k = mp->doc_id_k;
+    }
+    p.full_cnt = meta->full_cnt;
+    p.full_idx = meta->full_idx;
+    p.mask_cnt = meta->mask_cnt;
+    p.mask_idx = meta->mask_idx;
+    p.err = err_flag;
+    cudaError_t e = bsattn::launch_meta(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,
+                         int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, const bsattn_meta *meta,
+                         const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                         const bsattn_mask_params *mp, float softmax_scale, void *out, float *lse,
+                         int32_t *err_flag, void *stream) {
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
+    if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return BSATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
+    if (meta->B != B || meta->H != H) return BSATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+
+    bsattn::FwdParams p = {};
+    p.varlen = meta->varlen;
+    p.B = B;
+    p.H = H;
+    long long rows_q, rows_k;
+    if (meta->varlen) {
+        if (!cu_seqlens_q || !cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
+        if (kv_valid_len && meta->num_n <= 0) return BSATTN_ERR_INVALID_ARG;
+        rows_q = seqlen_q;
+        rows_k = seqlen_k;
+        p.total_m = meta->total_m_blocks;
+        p.total_n = meta->total_n_blocks;
+        p.lse_row_stride = seqlen_q;
+    } else {
+        if (cu_seqlens_q || cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
+        if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+            return BSATTN_ERR_INVALID_ARG;
+        rows_q = (long long)B * seqlen_q;
+        rows_k = (long long)B * seqlen_k;
+        p.total_m = B * meta->num_m;
+        p.num_m = meta->num_m;
+        p.num_n = meta->num_n;
+        p.lse_row_stride = seqlen_q;
+    }
+    if (rows_q > INT32_MAX || rows_k > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+    p.seqlen_q = seqlen_q;
+    p.seqlen_k = seqlen_k;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.full_cnt = meta->full_cnt;
+    p.full_idx = meta->full_idx;
+    p.mask_cnt = meta->mask_cnt;
+    p.mask_idx = meta->mask_idx;
+    p.cu_tm = meta->cu_total_m_blocks;
+    p.cu_off = meta->cu_block_idx_offsets;
+    p.vl = kv_valid_len;
+    p.vl_stride = meta->num_n;
+    p.kind = (int)kind;
+    if (mp) {
+        p.window_left = mp->window_left;
+        p.sink_tokens = mp->sink_tokens;
+        p.prefix_len = mp->prefix_len;
+        p.doc_q = mp->doc_id_q;
+        p.doc_k = mp->doc_id_k;
+    }
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
+    p.out = static_cast<uint16_t *>(out);
+    p.lse = lse;
+    p.err = err_flag;
+    p.pairs_per_head = (int)cdiv(p.total_m, 2);
+    if ((long long)H * p.pairs_per_head > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+    p.num_units = H * p.pairs_per_head;
+    if (p.num_units == 0 || rows_q == 0) return BSATTN_OK;
+
+    CUtensorMap tq, tk, tv;
+    if (!encode_bshd(&tq, q, rows_q, H, D) || !encode_bshd(&tk, k, rows_k > 0 ? rows_k : 1, H, D) ||
+        !encode_bshd(&tv, v, rows_k > 0 ? rows_k : 1, H, D))
+        return BSATTN_ERR_CUDA;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return BSATTN_ERR_CUDA;
+    cudaError_t e = bsattn::launch_fwd(p, tq, tk, tv, D, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,714 @@
+// Block-sparse attention forward for sm_103a: TMA + tcgen05 + TMEM, persistent,
+// warp-specialised.
+//
+// What it computes ("[CuTe,Flex] varlen blocksparsity", flash-attention #2224):
+// for each (head, Q tile) it visits only the KV tiles of the row's mask list and
+// full list, runs an online softmax over them (mask_mod only on mask tiles) and
+// writes O and LSE.  The K/V loads follow the listed blocks ("Dense
+// FlashAttention vs Block-Sparse Attention", sections 4 and 6: the next tile's
+// address is only known from the list) and both K and V jump to each listed tile.
+//
+// Work unit = (head, pair of consecutive packed Q tiles).  The two tiles' lists
+// are merged on the fly, largest global KV row first; a KV tile listed by both
+// tiles is loaded once and used by both (the paired 128-row halves of a 256-token
+// VSA block share their whole list; neighbouring sliding-window tiles share all
+// but one tile).
+//
+// Roles (384 threads, one CTA per SM, all of TMEM):
+//   warp 0      TMA producer: walks the lists (next index read one step ahead),
+//               loads Q tiles and K/V tiles into rings of shared-memory stages
+//   warp 1      tcgen05 issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P in TMEM
+//   warp 2      owns the TMEM allocation
+//   warps 4-7   softmax + O rescale + epilogue for tile 0 of the pair
+//   warps 8-11  the same for tile 1
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D);
+// P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+#include "bsattn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace bsattn {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+// Register split: the kernel is built for 168 registers per thread at launch
+// (65536 / 384, rounded down to a multiple of 8), i.e. 64512 for the CTA.  The
+// control warpgroup gives registers back and the two softmax warpgroups take
+// them: 128 * 72 + 2 * 128 * 216 = 64512, exactly the launch allocation.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kCtrlRegs = 72, kSoftmaxRegs = 216;
+static_assert(128 * kCtrlRegs + 2 * 128 * kSoftmaxRegs <= (uint32_t)kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr uint32_t kSubTileBytes = kTile * 64 * 2;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
+
+// Item flags (producer -> MMA issuer).
+constexpr uint32_t kPart0 = 1u, kPart1 = 2u, kMask0 = 4u, kMask1 = 8u, kEnd = 16u, kBound0 = 32u,
+                   kBound1 = 64u;
+// Per-tile flags (MMA issuer -> softmax).
+constexpr uint32_t kSMask = 1u, kSBound = 2u, kSEnd = 4u;
+
+struct Item {
+    int32_t krow;  // packed K/V row of the tile
+    int32_t n0, n1;
+    uint32_t flags;
+};
+
+struct SInfo {
+    int32_t n;
+    uint32_t flags;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kStagesK = D == 128 ? 2 : 4;
+    static constexpr int kStagesV = D == 128 ? 2 : 4;
+    static constexpr uint32_t kTileBytes = kTile * D * 2;
+    static constexpr int kSub = D / 64;  // 64-column swizzle spans per tile
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + 2 * kTileBytes;
+    static constexpr uint32_t kV = kK + kStagesK * kTileBytes;
+    static constexpr uint32_t kBar = kV + kStagesV * kTileBytes;
+    // barrier indices
+    static constexpr int bKF = 0, bKE = kStagesK, bVF = 2 * kStagesK, bVE = 2 * kStagesK + kStagesV;
+    static constexpr int bQF = 2 * kStagesK + 2 * kStagesV, bQE = bQF + 2, bSR = bQF + 4,
+                         bPR = bQF + 6, bOD = bQF + 8, bDrain = bQF + 10, kNumBars = bQF + 11;
+    static constexpr uint32_t kItems = kBar + kNumBars * 8;
+    static constexpr uint32_t kSInfo = kItems + kStagesK * sizeof(Item);
+    static constexpr uint32_t kMisc = kSInfo + 2 * sizeof(SInfo);  // [0] tmem base, [1] abort
+    static constexpr uint32_t kBytes = kMisc + 16;
+    static constexpr uint32_t kSmemAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct TileInfo {
+    int valid;
+    int b, m;
+    int qrow0;    // packed q row of the tile's first row
+    int nvalid;   // rows of the tile inside the sequence
+    int krow0;    // packed k row of the sequence's first key
+    int sk;       // seqlen_k(b)
+    int nn;       // num_n(b)
+    long long cnt_at, idx_at;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const FwdParams &p, int h, int T) {
+    TileInfo t;
+    t.valid = 0;
+    t.b = t.m = t.qrow0 = t.nvalid = t.krow0 = t.sk = t.nn = 0;
+    t.cnt_at = t.idx_at = 0;
+    if (T >= p.total_m) return t;
+    int sq;
+    if (!p.varlen) {
+        t.b = T / p.num_m;
+        t.m = T - t.b * p.num_m;
+        sq = p.seqlen_q;
+        t.sk = p.seqlen_k;
+        t.qrow0 = t.b * p.seqlen_q + t.m * kTile;
+        t.krow0 = t.b * p.seqlen_k;
+        t.nn = p.num_n;
+        t.cnt_at = ((long long)t.b * p.H + h) * p.num_m + t.m;
+        t.idx_at = t.cnt_at * p.num_n;
+    } else {
+        if (T >= p.cu_tm[p.B]) return t;
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu_tm[mid] <= T) lo = mid;
+            else hi = mid - 1;
+        }
+        t.b = lo;
+        t.m = T - p.cu_tm[lo];
+        sq = p.cu_q[lo + 1] - p.cu_q[lo];
+        t.sk = p.cu_k[lo + 1] - p.cu_k[lo];
+        t.qrow0 = p.cu_q[lo] + t.m * kTile;
+        t.krow0 = p.cu_k[lo];
+        t.nn = (t.sk + kTile - 1) / kTile;
+        t.cnt_at = (long long)h * p.total_m + T;
+        t.idx_at = (long long)h * p.total_n + p.cu_off[lo] + (long long)t.m * t.nn;
+        if ((long long)p.cu_off[lo] + (long long)(t.m + 1) * t.nn > p.total_n) return t;
+    }
+    t.nvalid = sq - t.m * kTile;
+    if (t.nvalid > kTile) t.nvalid = kTile;
+    if (t.nvalid <= 0) return t;
+    t.valid = 1;
+    return t;
+}
+
+// Bits [lo, hi) of a 32-bit word (positions relative to the word; clamped).
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > 32 ? 32 : hi;
+    if (hi <= lo) return 0u;
+    const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return below_hi & ~((1u << lo) - 1u);
+}
+
+// A list cursor whose next raw entry is loaded one step before it is needed.
+struct Cursor {
+    const int32_t *ptr;
+    int cnt, pos, head, pre;
+};
+
+__device__ __forceinline__ void cur_advance(Cursor &c, int nn, int32_t *err) {
+    while (true) {
+        ++c.pos;
+        if (c.pos >= c.cnt) {
+            c.head = -1;
+            return;
+        }
+        c.head = c.pre;
+        c.pre = (c.pos + 1 < c.cnt) ? __ldg(c.ptr + c.pos + 1) : -1;
+        if (c.head >= 0 && c.head < nn) return;
+        if (err) atomicOr(err, BSATTN_FLAG_BAD_INDEX);
+    }
+}
+
+__device__ __forceinline__ void cur_init(Cursor &c, const int32_t *ptr, int cnt, int nn,
+                                         int32_t *err) {
+    if (cnt < 0 || cnt > nn) {
+        if (err) atomicOr(err, BSATTN_FLAG_BAD_COUNT);
+        cnt = cnt < 0 ? 0 : nn;
+    }
+    c.ptr = ptr;
+    c.cnt = cnt;
+    c.pos = -1;
+    c.pre = cnt > 0 ? __ldg(ptr) : -1;
+    cur_advance(c, nn, err);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bsattn_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tq,
+                      const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    Item *items = reinterpret_cast<Item *>(gbase + C::kItems);
+    SInfo *sinfo = reinterpret_cast<SInfo *>(gbase + C::kSInfo);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + C::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    auto bar = [&](int i) -> uint32_t { return base + C::kBar + 8u * (uint32_t)i; };
+    const uint32_t sQ = base + C::kQ, sK = base + C::kK, sV = base + C::kV;
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStagesK; ++s) {
+            mbar_init(bar(C::bKF + s), 1);
+            mbar_init(bar(C::bKE + s), 1);
+        }
+        for (int s = 0; s < C::kStagesV; ++s) {
+            mbar_init(bar(C::bVF + s), 1);
+            mbar_init(bar(C::bVE + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::bQF + t), 1);
+            mbar_init(bar(C::bQE + t), 1);
+            mbar_init(bar(C::bSR + t), 2);
+            mbar_init(bar(C::bPR + t), 4);
+            mbar_init(bar(C::bOD + t), 1);
+        }
+        mbar_init(bar(C::bDrain), 1);
+        misc[1] = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(base + C::kMisc, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < 4) regs_release<kCtrlRegs>();
+    if (warp == 0) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            // Per-stage bit masks: was the full barrier ever armed, and the parity of
+            // its most recently armed phase (for the drain at the end).
+            uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0, q_armed = 0, q_par = 0;
+            uint32_t kc = 0, vc = 0, uc = 0;
+            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+                const int h = u / p.pairs_per_head;
+                const int pr = u - h * p.pairs_per_head;
+                TileInfo ti[2] = {tile_info(p, h, 2 * pr), tile_info(p, h, 2 * pr + 1)};
+                for (int t = 0; t < 2; ++t) {
+                    if (!mbar_wait(bar(C::bQE + t), (uc & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        goto producer_done;
+                    if (ti[t].valid) {
+                        mbar_arrive_expect_tx(bar(C::bQF + t), C::kTileBytes);
+                        for (int x = 0; x < C::kSub; ++x)
+                            tma_load_3d(sQ + t * C::kTileBytes + x * kSubTileBytes, &tq,
+                                        bar(C::bQF + t), x * 64, h, ti[t].qrow0);
+                        q_armed |= 1u << t;
+                        q_par = (q_par & ~(1u << t)) | ((uc & 1u) << t);
+                    } else {
+                        mbar_arrive(bar(C::bQF + t));
+                    }
+                }
+                Cursor cm[2], cf[2];
+                for (int t = 0; t < 2; ++t) {
+                    if (ti[t].valid) {
+                        cur_init(cm[t], p.mask_idx + ti[t].idx_at, __ldg(p.mask_cnt + ti[t].cnt_at),
+                                 ti[t].nn, p.err);
+                        cur_init(cf[t], p.full_idx + ti[t].idx_at, __ldg(p.full_cnt + ti[t].cnt_at),
+                                 ti[t].nn, p.err);
+                    } else {
+                        cm[t].head = cf[t].head = -1;
+                        cm[t].cnt = cf[t].cnt = 0;
+                        cm[t].pos = cf[t].pos = 0;
+                    }
+                }
+                while (true) {
+                    const int c0 = max(cm[0].head, cf[0].head);
+                    const int c1 = max(cm[1].head, cf[1].head);
+                    if (c0 < 0 && c1 < 0) break;
+                    const long long g0 = c0 >= 0 ? (long long)ti[0].krow0 + (long long)c0 * kTile : -1;
+                    const long long g1 = c1 >= 0 ? (long long)ti[1].krow0 + (long long)c1 * kTile : -1;
+                    const bool p0 = c0 >= 0 && g0 >= g1;
+                    const bool p1 = c1 >= 0 && g1 >= g0;
+                    Item it;
+                    it.krow = (int32_t)(p0 ? g0 : g1);
+                    it.n0 = p0 ? c0 : -1;
+                    it.n1 = p1 ? c1 : -1;
+                    it.flags = 0;
+                    if (p0) {
+                        it.flags |= kPart0;
+                        if (cm[0].head == c0) {
+                            it.flags |= kMask0;
+                            cur_advance(cm[0], ti[0].nn, p.err);
+                        } else {
+                            cur_advance(cf[0], ti[0].nn, p.err);
+                        }
+                        if ((c0 + 1) * kTile > ti[0].sk) it.flags |= kBound0;
+                    }
+                    if (p1) {
+                        it.flags |= kPart1;
+                        if (cm[1].head == c1) {
+                            it.flags |= kMask1;
+                            cur_advance(cm[1], ti[1].nn, p.err);
+                        } else {
+                            cur_advance(cf[1], ti[1].nn, p.err);
+                        }
+                        if ((c1 + 1) * kTile > ti[1].sk) it.flags |= kBound1;
+                    }
+                    const uint32_t ks = kc % C::kStagesK;
+                    if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        goto producer_done;
+                    items[ks] = it;
+                    mbar_arrive_expect_tx(bar(C::bKF + ks), C::kTileBytes);
+                    for (int x = 0; x < C::kSub; ++x)
+                        tma_load_3d(sK + ks * C::kTileBytes + x * kSubTileBytes, &tk, bar(C::bKF + ks),
+                                    x * 64, h, it.krow);
+                    k_armed |= 1u << ks;
+                    k_par = (k_par & ~(1u << ks)) | (((kc / C::kStagesK) & 1u) << ks);
+                    ++kc;
+                    const uint32_t vs = vc % C::kStagesV;
+                    if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        goto producer_done;
+                    mbar_arrive_expect_tx(bar(C::bVF + vs), C::kTileBytes);
+                    for (int x = 0; x < C::kSub; ++x)
+                        tma_load_3d(sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
+                                    x * 64, h, it.krow);
+                    v_armed |= 1u << vs;
+                    v_par = (v_par & ~(1u << vs)) | (((vc / C::kStagesV) & 1u) << vs);
+                    ++vc;
+                }
+                {
+                    const uint32_t ks = kc % C::kStagesK;
+                    if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        goto producer_done;
+                    Item end;
+                    end.krow = 0;
+                    end.n0 = end.n1 = -1;
+                    end.flags = kEnd;
+                    items[ks] = end;
+                    mbar_arrive(bar(C::bKF + ks));
+                    ++kc;
+                }
+            }
+        producer_done:
+            // Make sure no TMA write into this CTA's shared memory is still in flight.
+#pragma unroll
+            for (int s = 0; s < C::kStagesK; ++s)
+                if ((k_armed >> s) & 1u) mbar_wait_drain(bar(C::bKF + s), (k_par >> s) & 1u);
+#pragma unroll
+            for (int s = 0; s < C::kStagesV; ++s)
+                if ((v_armed >> s) & 1u) mbar_wait_drain(bar(C::bVF + s), (v_par >> s) & 1u);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if ((q_armed >> t) & 1u) mbar_wait_drain(bar(C::bQF + t), (q_par >> t) & 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+            uint32_t kc = 0, vc = 0, uc = 0;
+            uint32_t pc[2] = {0, 0};
+            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+                bool have_q[2] = {false, false};
+                bool first_pv[2] = {true, true};
+                int pend[2] = {-1, -1};  // V-ring item counter of the tile's pending P.V
+                bool ok = true;
+                // O_t += P_t V for the tile's pending item.
+                auto issue_pv = [&](int t) -> bool {
+                    if (!mbar_wait(bar(C::bPR + t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                        return false;
+                    ++pc[t];
+                    const uint32_t vcx = (uint32_t)pend[t];
+                    const uint32_t vs = vcx % C::kStagesV;
+                    if (!mbar_wait(bar(C::bVF + vs), (vcx / C::kStagesV) & 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t vbase = sV + vs * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, kSubTileBytes, 1024);
+                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
+                               (kk > 0 || !first_pv[t]) ? 1u : 0u);
+                    }
+                    first_pv[t] = false;
+                    mma_commit(bar(C::bOD + t));
+                    if (pend[1 - t] != pend[t]) mma_commit(bar(C::bVE + vs));
+                    pend[t] = -1;
+                    return true;
+                };
+                while (ok) {
+                    const uint32_t ks = kc % C::kStagesK;
+                    if (!mbar_wait(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    Item it;
+                    {
+                        const volatile Item *vi = &items[ks];
+                        it.krow = vi->krow;
+                        it.n0 = vi->n0;
+                        it.n1 = vi->n1;
+                        it.flags = vi->flags;
+                    }
+                    if (it.flags & kEnd) {
+                        for (int t = 0; t < 2 && ok; ++t)
+                            if (pend[t] >= 0) ok = issue_pv(t);
+                        for (int t = 0; t < 2 && ok; ++t)
+                            if (!have_q[t])
+                                ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                               BSATTN_FLAG_TIMEOUT);
+                        if (!ok) break;
+                        for (int t = 0; t < 2; ++t) mma_commit(bar(C::bQE + t));
+                        mbar_arrive(bar(C::bKE + ks));
+                        for (int t = 0; t < 2; ++t) {
+                            sinfo[t].n = -1;
+                            sinfo[t].flags = kSEnd;
+                            mma_commit(bar(C::bSR + t));
+                            mbar_arrive(bar(C::bSR + t));
+                        }
+                        ++kc;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!(it.flags & (t ? kPart1 : kPart0))) continue;
+                        if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
+                        if (!have_q[t]) {
+                            if (!(ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                                 BSATTN_FLAG_TIMEOUT)))
+                                break;
+                            have_q[t] = true;
+                            tc_fence_after();
+                        }
+                        const uint32_t qbase = sQ + t * C::kTileBytes;
+                        const uint32_t kbase = sK + ks * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kSubTileBytes + (kk & 3) * 32;
+                            mma_ss(tmem + t * 128, smem_desc_sw128(qbase + off, 16, 1024),
+                                   smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        sinfo[t].n = t ? it.n1 : it.n0;
+                        sinfo[t].flags = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
+                                         ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
+                        mma_commit(bar(C::bSR + t));
+                        mbar_arrive(bar(C::bSR + t));
+                        pend[t] = (int)vc;
+                    }
+                    if (!ok) break;
+                    // A tile that sits this item out retires its pending P.V now, so a
+                    // V stage is never held across more than one item.
+                    for (int t = 0; t < 2 && ok; ++t)
+                        if (!(it.flags & (t ? kPart1 : kPart0)) && pend[t] >= 0) ok = issue_pv(t);
+                    if (!ok) break;
+                    mma_commit(bar(C::bKE + ks));
+                    ++kc;
+                    ++vc;
+                }
+                if (!ok) break;
+            }
+            // Wait until every tcgen05 operation issued above has completed.
+            mma_commit(bar(C::bDrain));
+            mbar_wait_drain(bar(C::bDrain), 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- softmax --
+        regs_claim<kSoftmaxRegs>();
+        const int t = (warp >= 8) ? 1 : 0;
+        const uint32_t quarter = warp & 3u;
+        const int r = (int)(quarter * 32 + lane);                 // row of the tile
+        const uint32_t lane_addr = tmem + ((quarter * 32u) << 16);
+        const uint32_t s_col = (uint32_t)t * 128u;
+        const uint32_t o_col = 256u + (uint32_t)t * D;
+        const float sl2 = p.scale_log2;
+        uint32_t scount = 0, pvcount = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const int h = u / p.pairs_per_head;
+            const int pr = u - h * p.pairs_per_head;
+            const TileInfo ti = tile_info(p, h, 2 * pr + t);
+            const int i_seq = ti.m * kTile + r;  // sequence-local query position
+            float m_run = -INFINITY, l_run = 0.f;
+            int j = 0;
+            bool ok = true;
+            while (true) {
+                ok = mbar_wait(bar(C::bSR + t), scount & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++scount;
+                tc_fence_after();
+                SInfo si;
+                {
+                    const volatile SInfo *vs = &sinfo[t];
+                    si.n = vs->n;
+                    si.flags = vs->flags;
+                }
+                if (si.flags & kSEnd) break;
+
+                float s[128];
+                {
+                    uint32_t v0[32], v1[32], v2[32], v3[32];
+                    tmem_ld32(lane_addr + s_col + 0, v0);
+                    tmem_ld32(lane_addr + s_col + 32, v1);
+                    tmem_ld32(lane_addr + s_col + 64, v2);
+                    tmem_ld32(lane_addr + s_col + 96, v3);
+                    tmem_wait_ld();
+                    reg_fence(v0);
+                    reg_fence(v1);
+                    reg_fence(v2);
+                    reg_fence(v3);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        s[x] = __uint_as_float(v0[x]);
+                        s[32 + x] = __uint_as_float(v1[x]);
+                        s[64 + x] = __uint_as_float(v2[x]);
+                        s[96 + x] = __uint_as_float(v3[x]);
+                    }
+                }
+                if (si.flags & (kSMask | kSBound)) {
+                    // Keep-mask of the 128 columns as four 32-bit words, then one pass
+                    // that sets the dropped scores to -inf.
+                    const int j0 = si.n * kTile;
+                    int lim = min(kTile, ti.sk - j0);  // keys inside the sequence
+                    uint32_t keep[4];
+                    if (!(si.flags & kSMask)) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) keep[w] = span_bits(0, lim - 32 * w);
+                    } else {
+                        if (p.vl) lim = min(lim, __ldg(p.vl + (long long)ti.b * p.vl_stride + si.n));
+                        if (p.kind == BSATTN_MASK_DOCUMENT) {
+                            const int32_t dq = __ldg(p.doc_q + ti.qrow0 + min(r, ti.nvalid - 1));
+                            const int32_t *dk = p.doc_k + (long long)ti.krow0 + j0;
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t bits = 0;
+#pragma unroll 1
+                                for (int x = 0; x < 32; ++x) {
+                                    const int c = 32 * w + x;
+                                    if (c < lim && __ldg(dk + c) == dq) bits |= 1u << x;
+                                }
+                                keep[w] = bits;
+                            }
+                        } else {
+                            const int diag = i_seq - j0 + 1;  // columns c < diag have j <= i
+                            int la = 0, ha = lim, hb = 0;
+                            if (p.kind == BSATTN_MASK_CAUSAL) {
+                                ha = min(lim, diag);
+                            } else if (p.kind == BSATTN_MASK_SLIDING_WINDOW) {
+                                la = diag <= p.window_left ? 0 : diag - p.window_left;
+                                ha = min(lim, diag);
+                                hb = min(ha, p.sink_tokens - j0);
+                            } else if (p.kind == BSATTN_MASK_PREFIX) {
+                                ha = min(lim, max(p.prefix_len - j0, diag));
+                            }
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                keep[w] = span_bits(la - 32 * w, ha - 32 * w) | span_bits(0, hb - 32 * w);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (!((keep[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                // Rescale O only when some row's running maximum grew by more than 2^8;
+                // otherwise keep the stale maximum (O / l at the end is the same).
+                const bool rescale = (j > 0) && __any_sync(0xffffffffu, (m_new - m_run) > 8.0f);
+                float alpha = 1.f;
+                if (j == 0 || rescale) {
+                    if (rescale && m_new != -INFINITY) alpha = ex2_approx(m_run - m_new);
+                    m_run = m_new;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const float p0 = ex2_approx(fmaf(s[c * 64 + 2 * x], sl2, -m_use));
+                        const float p1 = ex2_approx(fmaf(s[c * 64 + 2 * x + 1], sl2, -m_use));
+                        l0 += p0;
+                        l1 += p1;
+                        pk[x] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(lane_addr + s_col + c * 32, pk);
+                }
+                l_run = l_run * alpha + (l0 + l1);
+                if (rescale) {
+                    // O_t must hold the previous item's P.V before it is rescaled.
+                    ok = mbar_wait(bar(C::bOD + t), (pvcount - 1) & 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(lane_addr + o_col + c * 32, v);
+                        tmem_wait_ld();
+                        reg_fence(v);
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
+                        tmem_st32(lane_addr + o_col + c * 32, v);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::bPR + t));
+                ++pvcount;
+                ++j;
+            }
+            if (!ok) break;
+            // Epilogue: O / l in bf16 and LSE = ln(sum of exp(scale * s)).
+            const bool row_ok = ti.valid && r < ti.nvalid;
+            uint16_t *orow = p.out + ((long long)(ti.qrow0 + r) * p.H + h) * D;
+            const bool empty = (j == 0) || !(l_run > 0.f);
+            const float inv = empty ? 0.f : 1.f / l_run;
+            if (j > 0) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_addr + o_col + c * 32, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
+                    if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv,
+                                              __uint_as_float(v[q4 * 8 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv,
+                                              __uint_as_float(v[q4 * 8 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv,
+                                              __uint_as_float(v[q4 * 8 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv,
+                                              __uint_as_float(v[q4 * 8 + 7]) * inv);
+                            dst[q4] = w;
+                        }
+                    }
+                }
+            } else if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow);
+                for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
+            }
+            if (row_ok) {
+                const float lse = empty ? -INFINITY : (m_run * 0.69314718055994530942f + logf(l_run));
+                const long long li = p.varlen
+                                         ? (long long)h * p.lse_row_stride + ti.qrow0 + r
+                                         : ((long long)ti.b * p.H + h) * p.lse_row_stride +
+                                               (long long)ti.m * kTile + r;
+                p.lse[li] = lse;
+            }
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
+    using C = Cfg<D>;
+    static int attr_set_for_device[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set_for_device[dev]) {
+        // The register split inside the kernel assumes exactly kLaunchRegs per
+        // thread at launch; refuse to run a build where that does not hold.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set_for_device[dev] = 1;
+    }
+    if (p.num_units <= 0) return cudaSuccess;
+    const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+    bsattn_fwd_kernel<D><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, int D, int num_sms, cudaStream_t stream) {
+    if (D == 128) return launch_fwd_d<128>(p, tq, tk, tv, num_sms, stream);
+    if (D == 64) return launch_fwd_d<64>(p, tq, tk, tv, num_sms, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bsattn

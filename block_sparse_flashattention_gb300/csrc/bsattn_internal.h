@@ -1,0 +1,56 @@
+// Parameters passed from the C-ABI entry points to the kernels (internal).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bsattn.h"
+
+namespace bsattn {
+
+constexpr int kTile = 128;  // tile_m = tile_n = 128 in this build
+
+struct MetaParams {
+    const uint8_t *map;
+    int varlen, B, H;
+    int num_m, num_n;              // batched sizes (varlen: num_n = kv_valid_len stride)
+    int total_m, total_n;          // varlen packed sizes as allocated by the caller
+    int seqlen_q, seqlen_k;        // batched
+    const int32_t *cu_q, *cu_k;    // varlen [B+1]
+    int32_t *cu_tm, *cu_off;       // varlen [B+1], written by the offsets kernel
+    const int32_t *vl;             // [B, vl_stride] or null
+    int vl_stride;
+    int kind, window_left, sink_tokens, prefix_len;
+    const int32_t *doc_q, *doc_k;
+    int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;
+    int32_t *err;
+};
+
+struct FwdParams {
+    int varlen, B, H;
+    int seqlen_q, seqlen_k;        // batched per-sequence lengths
+    const int32_t *cu_q, *cu_k;    // varlen [B+1]
+    int num_m, num_n;              // batched
+    int total_m, total_n;          // Q tiles per head over the batch; varlen idx row size
+    const int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;
+    const int32_t *cu_tm, *cu_off; // varlen
+    const int32_t *vl;
+    int vl_stride;
+    int kind, window_left, sink_tokens, prefix_len;
+    const int32_t *doc_q, *doc_k;
+    float scale_log2;              // softmax_scale * log2(e)
+    uint16_t *out;                 // bf16 bits
+    float *lse;
+    int32_t *err;
+    int lse_row_stride;            // batched: seqlen_q; varlen: total q rows
+    int pairs_per_head;            // ceil(total_m / 2)
+    int num_units;                 // H * pairs_per_head
+};
+
+cudaError_t launch_meta(const MetaParams &p, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, int D, int num_sms, cudaStream_t stream);
+
+}  // namespace bsattn

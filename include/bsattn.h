@@ -1,0 +1,168 @@
+/*
+ * bsattn -- block-sparse attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is caller-owned memory; the library allocates
+ * nothing and keeps no state between calls.  Device pointers must be CUDA
+ * device memory on the current device.  Calls are asynchronous on `stream`
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream) and never
+ * synchronise with the host.  The returned status covers host-side argument
+ * validation and kernel-launch errors only; faults in the metadata that only the
+ * device can see are reported through the optional `err_flag` word (bits
+ * BSATTN_FLAG_*), which the kernels OR into and never clear.  No kernel traps.
+ *
+ * Sources for the operations (page titles and the part of the page):
+ *  - "[CuTe,Flex] varlen blocksparsity", flash-attention pull request #2224:
+ *    description (batched and varlen-packed *_block_cnt / *_block_idx shapes,
+ *    num_m(b), num_n(b), total_m_blocks, total_n_blocks) and review thread
+ *    (metadata tuple (mask_block_cnt, mask_block_idx, full_block_cnt,
+ *    full_block_idx); cu_total_m_blocks and cu_block_idx_offsets, the latter
+ *    the running sum of num_m(b) * num_n(b); mask_mod only on mask blocks).
+ *  - "Dense FlashAttention vs Block-Sparse Attention" (learning note on
+ *    Block-Sparse-Attention), sections 2 and 4: boolean block rows become
+ *    reversed index lists padded with -1; the kernel walks only the listed
+ *    blocks and the K/V loads jump to each listed block.
+ *  - "[feat] VSA-256 fastpath on Blackwell via FA4 CuTe block-sparse
+ *    attention" (FastVideo #1354): Q/K/V in BSHD layout; a per-KV-block valid
+ *    length read by mask_mod; LSE in [B, H, S] layout.
+ */
+#ifndef BSATTN_H
+#define BSATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BSATTN_ABI_VERSION 1
+
+typedef enum {
+    BSATTN_OK = 0,
+    BSATTN_ERR_INVALID_ARG = 1, /* a pointer, size or layout argument is invalid     */
+    BSATTN_ERR_UNSUPPORTED = 2, /* valid, but not served by this build (e.g. D=96)   */
+    BSATTN_ERR_CUDA = 3         /* a CUDA call or a kernel launch failed             */
+} bsattn_status;
+
+/* Token-level mask_mod applied on mask-list blocks.  Positions are
+ * sequence-local: i = query position, j = key position inside the sequence. */
+typedef enum {
+    BSATTN_MASK_NONE = 0,           /* all keys                                      */
+    BSATTN_MASK_CAUSAL = 1,         /* j <= i                                        */
+    BSATTN_MASK_SLIDING_WINDOW = 2, /* j <= i && (i - j < window_left || j < sink_tokens) */
+    BSATTN_MASK_DOCUMENT = 3,       /* doc_id_q[q row] == doc_id_k[k row]            */
+    BSATTN_MASK_PREFIX = 4          /* j < prefix_len || j <= i                      */
+} bsattn_mask_kind;
+
+/* Device-side error bits ORed into *err_flag. */
+#define BSATTN_FLAG_BAD_COUNT 0x1   /* a block count outside [0, num_n(b)] was clamped        */
+#define BSATTN_FLAG_BAD_INDEX 0x2   /* a block index outside [0, num_n(b)) was skipped        */
+#define BSATTN_FLAG_TIMEOUT 0x4     /* a pipeline wait exceeded its limit; the CTA stopped   */
+#define BSATTN_FLAG_BAD_SEQLENS 0x8 /* cu_seqlens disagree with the sizes given in the meta  */
+
+typedef struct {
+    int32_t window_left;      /* SLIDING_WINDOW: keys with 0 <= i - j < window_left      */
+    int32_t sink_tokens;      /* SLIDING_WINDOW: keys j < sink_tokens (still causal)     */
+    int32_t prefix_len;       /* PREFIX: keys j < prefix_len, else causal                */
+    const int32_t *doc_id_q;  /* DOCUMENT: device int32, one id per packed q row        */
+    const int32_t *doc_id_k;  /* DOCUMENT: device int32, one id per packed k row        */
+} bsattn_mask_params;
+
+/*
+ * Block-sparse metadata (all arrays device int32, caller-allocated).
+ *
+ * Batched (varlen = 0), sequences of equal length:
+ *   full_cnt, mask_cnt  [B, H, num_m]
+ *   full_idx, mask_idx  [B, H, num_m, num_n]
+ *   cu_total_m_blocks, cu_block_idx_offsets: unused (may be NULL)
+ * Varlen (varlen = 1), sequences packed back to back:
+ *   full_cnt, mask_cnt  [H, total_m_blocks]
+ *   full_idx, mask_idx  [H, total_n_blocks]; row (b, m) of head h starts at
+ *                       h * total_n_blocks + cu_block_idx_offsets[b] + m * num_n(b)
+ *   cu_total_m_blocks   [B+1], running sum of num_m(b)
+ *   cu_block_idx_offsets[B+1], running sum of num_m(b) * num_n(b)
+ *   num_m               unused; num_n = the row stride of kv_valid_len (at least
+ *                       the largest num_n(b))
+ * Each index row lists KV block ids in descending order; entries at and after
+ * the row's count are -1.  tile_m = tile_n = 128 in this build.
+ */
+typedef struct {
+    int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;
+    int32_t *cu_total_m_blocks, *cu_block_idx_offsets;
+    int32_t varlen, B, H, num_m, num_n;
+    int32_t total_m_blocks, total_n_blocks;
+    int32_t tile_m, tile_n;
+} bsattn_meta;
+
+/*
+ * bsattn_build_meta -- boolean block map -> full / mask lists (and, for
+ * varlen, the two offset tensors).
+ *
+ * Every selected KV tile n of row (b, h, m) is classified by the token
+ * predicate P(i, j) = j < seqlen_k(b) && mask_mod(i, j) && (j - 128 n) <
+ * kv_valid_len[b, n] over the tile's query rows i < seqlen_q(b) and its 128
+ * keys j: true for every pair -> full list, for some pair -> mask list, for none
+ * -> dropped.  Result is bit-exact and deterministic.
+ *
+ * block_map     device uint8; batched [B, H, num_m, num_n], varlen [H, total_n_blocks]
+ *               in the packed layout above; nonzero = selected.
+ * cu_seqlens_q  varlen: device int32 [B+1] packed row offsets; batched: NULL.
+ * cu_seqlens_k  likewise for keys.
+ * seqlen_q/_k   batched: per-sequence lengths (num_m == ceil(seqlen_q/128),
+ *               num_n == ceil(seqlen_k/128) is checked); varlen: ignored.
+ * kv_valid_len  optional device int32 [B, meta->num_n]: valid keys at the start
+ *               of each KV tile (the rest of the tile is masked on mask blocks).
+ * kind, mp      mask_mod (mp may be NULL unless the kind needs it).
+ * meta          sizes in, device output pointers in; varlen also writes
+ *               cu_total_m_blocks / cu_block_idx_offsets.  If the totals the
+ *               device computes differ from meta->total_*_blocks, rows past the
+ *               given totals are not written and BSATTN_FLAG_BAD_SEQLENS is set.
+ * err_flag      optional device int32 word (see BSATTN_FLAG_*).
+ */
+bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
+                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
+                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                int32_t *err_flag, void *stream);
+
+/*
+ * bsattn_fwd -- block-sparse attention forward.
+ *
+ * For each head h, sequence b and query row i (tile m = i / 128), the allowed
+ * key set is every key j < seqlen_k(b) of the tiles in the full list of row
+ * (b, h, m), plus every key of the tiles in its mask list that passes the token
+ * predicate of bsattn_build_meta.  Then, with s_j = softmax_scale * q_i . k_j,
+ *   lse_i = ln(sum_j exp(s_j)),  out_i = sum_j exp(s_j - lse_i) v_j,
+ * and an empty key set gives out_i = 0, lse_i = -inf.  Accumulation is fp32;
+ * the probabilities are rounded to bf16 before the P.V product.
+ *
+ * q             device bf16, batched [B, seqlen_q, H, D], varlen [seqlen_q, H, D]
+ *               (seqlen_q = total packed rows); contiguous, 16-byte aligned.
+ * k, v          device bf16, same layout with seqlen_k.
+ * B, H, D       D in {64, 128}; H equal for q and k/v.
+ * cu_seqlens_*  varlen: device int32 [B+1]; batched: NULL.
+ * meta          lists as written by bsattn_build_meta (or the caller, same format;
+ *               indices out of range are skipped and flagged).
+ * kv_valid_len, kind, mp   as for bsattn_build_meta (applied on mask-list tiles).
+ * softmax_scale > 0.
+ * out           device bf16, same shape as q.
+ * lse           device fp32, batched [B, H, seqlen_q], varlen [H, seqlen_q].
+ * err_flag      optional device int32 word.
+ */
+bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,
+                         int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, const bsattn_meta *meta,
+                         const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                         const bsattn_mask_params *mp, float softmax_scale, void *out, float *lse,
+                         int32_t *err_flag, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *bsattn_status_string(bsattn_status status);
+
+/* BSATTN_ABI_VERSION of the loaded library. */
+int32_t bsattn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSATTN_H */

@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports what include/bsattn.h declares, and rejects
+bad arguments on the host (no GPU needed: every case here fails validation
+before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_flashattention_gb300 as bsa
+from block_sparse_flashattention_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "bsattn.h")
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced here
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(bsattn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"bsattn_build_meta", "bsattn_fwd", "bsattn_status_string",
+            "bsattn_abi_version"} <= set(names)
+
+
+def test_library_exports_every_declared_function():
+    lib = ctypes.CDLL(_build.LIB)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared but not exported"
+
+
+def test_abi_version_and_status_strings():
+    text = open(HEADER).read()
+    ver = int(re.search(r"#define BSATTN_ABI_VERSION (\d+)", text).group(1))
+    assert bsa.bsattn_abi_version() == ver
+    assert bsa.status_string(bsa.BSATTN_OK) == "BSATTN_OK"
+    assert bsa.status_string(bsa.BSATTN_ERR_INVALID_ARG) == "BSATTN_ERR_INVALID_ARG"
+    assert bsa.status_string(bsa.BSATTN_ERR_UNSUPPORTED) == "BSATTN_ERR_UNSUPPORTED"
+    assert bsa.status_string(bsa.BSATTN_ERR_CUDA) == "BSATTN_ERR_CUDA"
+    assert bsa.status_string(99) == "BSATTN_ERR_UNKNOWN"
+
+
+def _meta(**kw):
+    base = dict(full_cnt=FAKE, full_idx=FAKE, mask_cnt=FAKE, mask_idx=FAKE, varlen=0, B=1, H=2,
+                num_m=2, num_n=2)
+    base.update(kw)
+    return bsa.Meta(**base)
+
+
+def _fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, seqlen_q=256, seqlen_k=256, H=2, D=128,
+             cu_seqlens_q=None, cu_seqlens_k=None, meta=_meta(), kv_valid_len=None,
+             kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, out=FAKE, lse=FAKE,
+             err_flag=None, stream=0)
+    a.update(kw)
+    return bsa.bsattn_fwd(**a)
+
+
+def _bm(**kw):
+    a = dict(block_map=FAKE, cu_seqlens_q=None, cu_seqlens_k=None, seqlen_q=256, seqlen_k=256,
+             kv_valid_len=None, kind=bsa.MASK_CAUSAL, mask_params=None, meta=_meta(),
+             err_flag=None, stream=0)
+    a.update(kw)
+    return bsa.bsattn_build_meta(**a)
+
+
+INV, UNS = bsa.BSATTN_ERR_INVALID_ARG, bsa.BSATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(D=96), UNS),
+    (dict(D=256), UNS),
+    (dict(q=FAKE + 2), INV),                       # not 16-byte aligned
+    (dict(out=None), INV),
+    (dict(lse=None), INV),
+    (dict(softmax_scale=0.0), INV),
+    (dict(softmax_scale=-1.0), INV),
+    (dict(softmax_scale=float("inf")), INV),
+    (dict(seqlen_q=300), INV),                     # num_m would be 3, meta says 2
+    (dict(B=2), INV),                              # meta.B disagrees
+    (dict(H=3), INV),
+    (dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE), INV),   # batched meta with cu_seqlens
+    (dict(meta=_meta(tile_m=64)), UNS),
+    (dict(meta=_meta(full_idx=None)), INV),
+    (dict(meta=_meta(varlen=1)), INV),             # varlen meta without offset tensors
+    (dict(kind=7), INV),
+    (dict(kind=bsa.MASK_SLIDING_WINDOW), INV),     # needs mask params
+    (dict(kind=bsa.MASK_DOCUMENT, mask_params=bsa.MaskParams()), INV),
+    (dict(kind=bsa.MASK_PREFIX, mask_params=bsa.MaskParams(prefix_len=-1)), INV),
+])
+def test_fwd_rejects_bad_arguments(kw, expect):
+    assert _fwd(**kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(block_map=None), INV),
+    (dict(seqlen_k=600), INV),
+    (dict(seqlen_q=-1), INV),
+    (dict(cu_seqlens_q=FAKE), INV),
+    (dict(meta=_meta(tile_n=256)), UNS),
+    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), INV),
+    (dict(kind=bsa.MASK_SLIDING_WINDOW, mask_params=bsa.MaskParams(window_left=-5)), INV),
+])
+def test_build_meta_rejects_bad_arguments(kw, expect):
+    assert _bm(**kw) == expect
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from block_sparse_flashattention_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.library()
