@@ -40,7 +40,7 @@ DEFAULT_CONFIG = 4
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG,
@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="keep only the first N heads (a smaller case for profiling)")
     return ap.parse_args()
 
 
@@ -234,6 +236,9 @@ def run_native(args):
         pg = dist
 
     wl = make_workload(args.config)
+    if args.heads:
+        from workloads.configs import with_heads
+        wl = with_heads(wl, args.heads)
     # inputs in pinned host memory (the e2e leg copies them every step)
     pin = dict(pin_memory=True)
     hq = torch.empty(wl.q_shape(), dtype=torch.int16, **pin)
@@ -278,7 +283,7 @@ def run_native(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(gpu_index_for_smi(torch, dev))
-    time.sleep(0.3)
+    time.sleep(0.5)   # the sampler is running before the timed region starts
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -355,10 +360,14 @@ def run_native(args):
     traffic = None
     prof = os.path.join(ROOT, "profiles", "bsattn_fwd_traffic.json")
     if os.path.exists(prof):
+        # the DRAM counters count only while the kernel source is the one profiled
+        import hashlib
+        src = os.path.join(ROOT, "block_sparse_flashattention_gb300", "csrc", "bsattn_fwd.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         try:
             with open(prof) as f:
                 tr = json.load(f)
-            if tr.get("workload") == wl.name:
+            if tr.get("workload") == wl.name and tr.get("kernel_sha256_prefix") == sha:
                 traffic = tr.get("bytes_per_launch")
         except (OSError, ValueError):
             traffic = None

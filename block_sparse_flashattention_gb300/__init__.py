@@ -16,6 +16,7 @@ from typing import Optional
 from ._binding import (BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUPPORTED,
                        BSATTN_OK, FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_BAD_SEQLENS, FLAG_TIMEOUT,
                        MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX, MASK_SLIDING_WINDOW,
+                       OUT_BF16, OUT_F32,
                        BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
                        bsattn_fwd, library, status_string)
 
@@ -23,7 +24,7 @@ TILE = 128
 
 __all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_abi_version", "alloc_meta", "build_meta",
            "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
-           "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
+           "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
            "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA",
            "FLAG_BAD_COUNT", "FLAG_BAD_INDEX", "FLAG_TIMEOUT", "FLAG_BAD_SEQLENS"]
 
@@ -76,11 +77,12 @@ def build_meta(block_map, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, s
 
 def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_valid_len=None,
             kind: int = MASK_NONE, mask_params: Optional[MaskParams] = None,
-            softmax_scale: Optional[float] = None, out=None, lse=None, err_flag=None,
-            stream=None):
+            softmax_scale: Optional[float] = None, out=None, out_dtype=None, lse=None,
+            err_flag=None, stream=None):
     """Block-sparse attention forward.  q/k/v: bf16 [B, S, H, D] or packed [total, H, D].
 
-    Returns (out, lse): out like q, lse fp32 [B, H, S_q] (batched) or [H, total_q]."""
+    Returns (out, lse): out shaped like q (bf16 by default, or torch.float32),
+    lse fp32 [B, H, S_q] (batched) or [H, total_q]."""
     import torch
     varlen = bool(meta.varlen)
     if varlen:
@@ -93,11 +95,18 @@ def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_val
         lse_shape = (meta.B, H, seqlen_q)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    elif out.dtype != out_dtype:
+        raise ValueError("out.dtype and out_dtype disagree")
     if lse is None:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     _check(bsattn_fwd(q, k, v, meta.B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta,
-                      kv_valid_len, kind, mask_params, softmax_scale, out, lse, err_flag, stream),
+                      kv_valid_len, kind, mask_params, softmax_scale, out,
+                      OUT_F32 if out_dtype == torch.float32 else OUT_BF16, lse, err_flag, stream),
            "bsattn_fwd")
     return out, lse

@@ -15,6 +15,7 @@ from ._build import LIB
 
 BSATTN_OK, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUPPORTED, BSATTN_ERR_CUDA = 0, 1, 2, 3
 MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 0, 1, 2, 3, 4
+OUT_BF16, OUT_F32 = 0, 1
 FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_TIMEOUT, FLAG_BAD_SEQLENS = 0x1, 0x2, 0x4, 0x8
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -62,8 +63,8 @@ def library() -> ctypes.CDLL:
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.POINTER(bsattn_meta), ctypes.c_void_p, ctypes.c_int,
-            ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
-            ctypes.c_void_p, ctypes.c_void_p]
+            ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_fwd.restype = ctypes.c_int
         lib.bsattn_status_string.argtypes = [ctypes.c_int]
         lib.bsattn_status_string.restype = ctypes.c_char_p
@@ -149,16 +150,16 @@ def bsattn_build_meta(block_map, cu_seqlens_q, cu_seqlens_k, seqlen_q: int, seql
 
 def bsattn_fwd(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int, cu_seqlens_q,
                cu_seqlens_k, meta: Meta, kv_valid_len, kind: int,
-               mask_params: Optional[MaskParams], softmax_scale: float, out, lse, err_flag=None,
-               stream=None) -> int:
+               mask_params: Optional[MaskParams], softmax_scale: float, out, out_dtype: int, lse,
+               err_flag=None, stream=None) -> int:
     """Forwards to the C function of the same name; returns its status code."""
     mp = mask_params.to_c() if mask_params is not None else None
     mt = meta.to_c()
     return library().bsattn_fwd(
         _ptr(q), _ptr(k), _ptr(v), int(B), int(seqlen_q), int(seqlen_k), int(H), int(D),
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), ctypes.byref(mt), _ptr(kv_valid_len), int(kind),
-        ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(out), _ptr(lse),
-        _ptr(err_flag), _stream(stream))
+        ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(out),
+        int(out_dtype), _ptr(lse), _ptr(err_flag), _stream(stream))
 
 
 def bsattn_abi_version() -> int:

@@ -171,8 +171,8 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
                          int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
                          const int32_t *cu_seqlens_k, const bsattn_meta *meta,
                          const int32_t *kv_valid_len, bsattn_mask_kind kind,
-                         const bsattn_mask_params *mp, float softmax_scale, void *out, float *lse,
-                         int32_t *err_flag, void *stream) {
+                         const bsattn_mask_params *mp, float softmax_scale, void *out,
+                         bsattn_out_dtype out_dtype, float *lse, int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
@@ -182,6 +182,7 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
     if (B <= 0 || H <= 0 || seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
     if (meta->B != B || meta->H != H) return BSATTN_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSATTN_ERR_INVALID_ARG;
+    if (out_dtype != BSATTN_OUT_BF16 && out_dtype != BSATTN_OUT_F32) return BSATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
 
     bsattn::FwdParams p = {};
@@ -230,7 +231,8 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
         p.doc_k = mp->doc_id_k;
     }
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
-    p.out = static_cast<uint16_t *>(out);
+    p.out = out;
+    p.out_f32 = out_dtype == BSATTN_OUT_F32 ? 1 : 0;
     p.lse = lse;
     p.err = err_flag;
     p.pairs_per_head = (int)cdiv(p.total_m, 2);

@@ -233,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
-            // Per-stage bit masks: was the full barrier ever armed, and the parity of
-            // its most recently armed phase (for the drain at the end).
-            uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0, q_armed = 0, q_par = 0;
-            uint32_t kc = 0, vc = 0, uc = 0;
+            // kc / vc count every use of a K / V stage (TMA arm or end marker); qn
+            // counts the uses of each Q stage.  The drain below derives from them the
+            // last phase of every full barrier.
+            uint32_t kc = 0, vc = 0, uc = 0, qn0 = 0, qn1 = 0;
             for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
                 const int h = u / p.pairs_per_head;
                 const int pr = u - h * p.pairs_per_head;
@@ -250,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int x = 0; x < C::kSub; ++x)
                             tma_load_3d(sQ + t * C::kTileBytes + x * kSubTileBytes, &tq,
                                         bar(C::bQF + t), x * 64, h, ti[t].qrow0);
-                        q_armed |= 1u << t;
-                        q_par = (q_par & ~(1u << t)) | ((uc & 1u) << t);
                     } else {
                         mbar_arrive(bar(C::bQF + t));
                     }
+                    if (t == 0) ++qn0;
+                    else ++qn1;
                 }
                 Cursor cm[2], cf[2];
                 for (int t = 0; t < 2; ++t) {
@@ -311,8 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < C::kSub; ++x)
                         tma_load_3d(sK + ks * C::kTileBytes + x * kSubTileBytes, &tk, bar(C::bKF + ks),
                                     x * 64, h, it.krow);
-                    k_armed |= 1u << ks;
-                    k_par = (k_par & ~(1u << ks)) | (((kc / C::kStagesK) & 1u) << ks);
                     ++kc;
                     const uint32_t vs = vc % C::kStagesV;
                     if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
@@ -322,8 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < C::kSub; ++x)
                         tma_load_3d(sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
                                     x * 64, h, it.krow);
-                    v_armed |= 1u << vs;
-                    v_par = (v_par & ~(1u << vs)) | (((vc / C::kStagesV) & 1u) << vs);
                     ++vc;
                 }
                 {
@@ -342,15 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         producer_done:
             // Make sure no TMA write into this CTA's shared memory is still in flight.
+            // Stage s was last used by item (kc - 1 - s) / kStages * kStages + s, whose
+            // phase is (kc - 1 - s) / kStages.
 #pragma unroll
-            for (int s = 0; s < C::kStagesK; ++s)
-                if ((k_armed >> s) & 1u) mbar_wait_drain(bar(C::bKF + s), (k_par >> s) & 1u);
+            for (uint32_t s = 0; s < (uint32_t)C::kStagesK; ++s)
+                if (kc > s) mbar_wait_drain(bar(C::bKF + s), ((kc - 1 - s) / C::kStagesK) & 1u);
 #pragma unroll
-            for (int s = 0; s < C::kStagesV; ++s)
-                if ((v_armed >> s) & 1u) mbar_wait_drain(bar(C::bVF + s), (v_par >> s) & 1u);
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if ((q_armed >> t) & 1u) mbar_wait_drain(bar(C::bQF + t), (q_par >> t) & 1u);
+            for (uint32_t s = 0; s < (uint32_t)C::kStagesV; ++s)
+                if (vc > s) mbar_wait_drain(bar(C::bVF + s), ((vc - 1 - s) / C::kStagesV) & 1u);
+            if (qn0 > 0) mbar_wait_drain(bar(C::bQF + 0), (qn0 - 1) & 1u);
+            if (qn1 > 0) mbar_wait_drain(bar(C::bQF + 1), (qn1 - 1) & 1u);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer --
@@ -624,36 +621,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // Epilogue: O / l in bf16 and LSE = ln(sum of exp(scale * s)).
             const bool row_ok = ti.valid && r < ti.nvalid;
-            uint16_t *orow = p.out + ((long long)(ti.qrow0 + r) * p.H + h) * D;
+            const long long orow = ((long long)(ti.qrow0 + r) * p.H + h) * D;  // element offset
             const bool empty = (j == 0) || !(l_run > 0.f);
             const float inv = empty ? 0.f : 1.f / l_run;
-            if (j > 0) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                if (j > 0) {
                     tmem_ld32(lane_addr + o_col + c * 32, v);
                     tmem_wait_ld();
                     reg_fence(v);
-                    if (row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                } else {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv,
-                                              __uint_as_float(v[q4 * 8 + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv,
-                                              __uint_as_float(v[q4 * 8 + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv,
-                                              __uint_as_float(v[q4 * 8 + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv,
-                                              __uint_as_float(v[q4 * 8 + 7]) * inv);
-                            dst[q4] = w;
-                        }
+                    for (int x = 0; x < 32; ++x) v[x] = 0u;
+                }
+                if (!row_ok) continue;
+                if (p.out_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        dst[q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv,
+                                              __uint_as_float(v[q4 * 4 + 1]) * inv,
+                                              __uint_as_float(v[q4 * 4 + 2]) * inv,
+                                              __uint_as_float(v[q4 * 4 + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + orow + c * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv,
+                                          __uint_as_float(v[q4 * 8 + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv,
+                                          __uint_as_float(v[q4 * 8 + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv,
+                                          __uint_as_float(v[q4 * 8 + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv,
+                                          __uint_as_float(v[q4 * 8 + 7]) * inv);
+                        dst[q4] = w;
                     }
                 }
-            } else if (row_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow);
-                for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
             }
             if (row_ok) {
                 const float lse = empty ? -INFINITY : (m_run * 0.69314718055994530942f + logf(l_run));

@@ -41,7 +41,8 @@ struct FwdParams {
     int kind, window_left, sink_tokens, prefix_len;
     const int32_t *doc_q, *doc_k;
     float scale_log2;              // softmax_scale * log2(e)
-    uint16_t *out;                 // bf16 bits
+    void *out;                     // bf16 or fp32 (out_f32)
+    int out_f32;
     float *lse;
     int32_t *err;
     int lse_row_stride;            // batched: seqlen_q; varlen: total q rows

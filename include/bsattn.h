@@ -53,6 +53,12 @@ typedef enum {
     BSATTN_MASK_PREFIX = 4          /* j < prefix_len || j <= i                      */
 } bsattn_mask_kind;
 
+/* Element type of the attention output. */
+typedef enum {
+    BSATTN_OUT_BF16 = 0, /* round-to-nearest-even of the fp32 result */
+    BSATTN_OUT_F32 = 1   /* the fp32 result itself                   */
+} bsattn_out_dtype;
+
 /* Device-side error bits ORed into *err_flag. */
 #define BSATTN_FLAG_BAD_COUNT 0x1   /* a block count outside [0, num_n(b)] was clamped        */
 #define BSATTN_FLAG_BAD_INDEX 0x2   /* a block index outside [0, num_n(b)) was skipped        */
@@ -144,7 +150,8 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
  *               indices out of range are skipped and flagged).
  * kv_valid_len, kind, mp   as for bsattn_build_meta (applied on mask-list tiles).
  * softmax_scale > 0.
- * out           device bf16, same shape as q.
+ * out           device, same shape as q; element type out_dtype.
+ * out_dtype     BSATTN_OUT_BF16 or BSATTN_OUT_F32.
  * lse           device fp32, batched [B, H, seqlen_q], varlen [H, seqlen_q].
  * err_flag      optional device int32 word.
  */
@@ -152,8 +159,8 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
                          int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
                          const int32_t *cu_seqlens_k, const bsattn_meta *meta,
                          const int32_t *kv_valid_len, bsattn_mask_kind kind,
-                         const bsattn_mask_params *mp, float softmax_scale, void *out, float *lse,
-                         int32_t *err_flag, void *stream);
+                         const bsattn_mask_params *mp, float softmax_scale, void *out,
+                         bsattn_out_dtype out_dtype, float *lse, int32_t *err_flag, void *stream);
 
 /* Human-readable name of a status code (static string). */
 const char *bsattn_status_string(bsattn_status status);

@@ -57,7 +57,8 @@ def _meta(**kw):
 def _fwd(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, seqlen_q=256, seqlen_k=256, H=2, D=128,
              cu_seqlens_q=None, cu_seqlens_k=None, meta=_meta(), kv_valid_len=None,
-             kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, out=FAKE, lse=FAKE,
+             kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, out=FAKE,
+             out_dtype=bsa.OUT_BF16, lse=FAKE,
              err_flag=None, stream=0)
     a.update(kw)
     return bsa.bsattn_fwd(**a)
@@ -79,6 +80,7 @@ INV, UNS = bsa.BSATTN_ERR_INVALID_ARG, bsa.BSATTN_ERR_UNSUPPORTED
     (dict(D=256), UNS),
     (dict(q=FAKE + 2), INV),                       # not 16-byte aligned
     (dict(out=None), INV),
+    (dict(out_dtype=7), INV),
     (dict(lse=None), INV),
     (dict(softmax_scale=0.0), INV),
     (dict(softmax_scale=-1.0), INV),

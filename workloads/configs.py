@@ -299,5 +299,14 @@ def _cfg5() -> Workload:
 CONFIGS = {1: _cfg1, 2: _cfg2, 3: _cfg3, 4: _cfg4, 5: _cfg5}
 
 
+def with_heads(wl: Workload, heads: int) -> Workload:
+    """The first `heads` heads of a workload's block map (q/k/v are drawn for the
+    new shape): a smaller case with the same sparsity structure, for profiling."""
+    from dataclasses import replace
+    bm = wl.block_map[:heads] if wl.varlen else wl.block_map[:, :heads]
+    return replace(wl, H=heads, block_map=np.ascontiguousarray(bm),
+                   name=f"{wl.name}_first{heads}heads")
+
+
 def make_workload(cfg: int) -> Workload:
     return CONFIGS[cfg]()
