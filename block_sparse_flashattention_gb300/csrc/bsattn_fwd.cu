@@ -35,9 +35,12 @@ constexpr uint32_t kTmemCols = 512;
 // Register split: the kernel is built for 168 registers per thread at launch
 // (65536 / 384, rounded down to a multiple of 8), i.e. 64512 for the CTA.  The
 // control warpgroup gives registers back and the two softmax warpgroups take
-// them: 128 * 72 + 2 * 128 * 216 = 64512, exactly the launch allocation.
+// them: 128 * 88 + 2 * 128 * 208 = 64512, exactly the launch allocation.
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kCtrlRegs = 72, kSoftmaxRegs = 216;
+constexpr int kStagesK128 = 2;  // K ring depth at d = 128 (3 measured no faster)
+// Issue tile 0's pending P.V before waiting for the next K tile (measured no faster).
+constexpr bool kPvBeforeK = false;
+constexpr uint32_t kCtrlRegs = 88, kSoftmaxRegs = 208;
 static_assert(128 * kCtrlRegs + 2 * 128 * kSoftmaxRegs <= (uint32_t)kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kSubTileBytes = kTile * 64 * 2;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
@@ -52,16 +55,21 @@ struct Item {
     int32_t krow;  // packed K/V row of the tile
     int32_t n0, n1;
     uint32_t flags;
+    int32_t lim0, lim1;  // per tile: keys of the tile that may be kept (sequence end,
+                         // and the valid length on mask tiles)
+    int32_t pad0, pad1;
 };
 
 struct SInfo {
     int32_t n;
     uint32_t flags;
+    int32_t lim;
+    int32_t pad;
 };
 
 template <int D>
 struct Cfg {
-    static constexpr int kStagesK = D == 128 ? 2 : 4;
+    static constexpr int kStagesK = D == 128 ? kStagesK128 : 4;
     static constexpr int kStagesV = D == 128 ? 2 : 4;
     static constexpr uint32_t kTileBytes = kTile * D * 2;
     static constexpr int kSub = D / 64;  // 64-column swizzle spans per tile
@@ -72,7 +80,7 @@ struct Cfg {
     // barrier indices
     static constexpr int bKF = 0, bKE = kStagesK, bVF = 2 * kStagesK, bVE = 2 * kStagesK + kStagesV;
     static constexpr int bQF = 2 * kStagesK + 2 * kStagesV, bQE = bQF + 2, bSR = bQF + 4,
-                         bPR = bQF + 6, bOD = bQF + 8, bDrain = bQF + 10, kNumBars = bQF + 11;
+                         bPR = bQF + 6, bDrain = bQF + 10, kNumBars = bQF + 11;  // bPR + 2t + half
     static constexpr uint32_t kItems = kBar + kNumBars * 8;
     static constexpr uint32_t kSInfo = kItems + kStagesK * sizeof(Item);
     static constexpr uint32_t kMisc = kSInfo + 2 * sizeof(SInfo);  // [0] tmem base, [1] abort
@@ -209,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::bQF + t), 1);
             mbar_init(bar(C::bQE + t), 1);
             mbar_init(bar(C::bSR + t), 2);
-            mbar_init(bar(C::bPR + t), 4);
-            mbar_init(bar(C::bOD + t), 1);
+            mbar_init(bar(C::bPR + 2 * t), 4);      // first half of P_t: one arrival per warp
+            mbar_init(bar(C::bPR + 2 * t + 1), 4);  // second half
         }
         mbar_init(bar(C::bDrain), 1);
         misc[1] = 0;
@@ -282,10 +290,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     it.n0 = p0 ? c0 : -1;
                     it.n1 = p1 ? c1 : -1;
                     it.flags = 0;
+                    it.lim0 = it.lim1 = kTile;
+                    it.pad0 = it.pad1 = 0;
+                    int vl0 = kTile, vl1 = kTile;  // valid lengths, loaded before the stage wait
                     if (p0) {
                         it.flags |= kPart0;
                         if (cm[0].head == c0) {
                             it.flags |= kMask0;
+                            if (p.vl) vl0 = __ldg(p.vl + (long long)ti[0].b * p.vl_stride + c0);
                             cur_advance(cm[0], ti[0].nn, p.err);
                         } else {
                             cur_advance(cf[0], ti[0].nn, p.err);
@@ -296,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.flags |= kPart1;
                         if (cm[1].head == c1) {
                             it.flags |= kMask1;
+                            if (p.vl) vl1 = __ldg(p.vl + (long long)ti[1].b * p.vl_stride + c1);
                             cur_advance(cm[1], ti[1].nn, p.err);
                         } else {
                             cur_advance(cf[1], ti[1].nn, p.err);
@@ -306,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
                         goto producer_done;
+                    if (p0) it.lim0 = min(min(kTile, ti[0].sk - c0 * kTile), vl0);
+                    if (p1) it.lim1 = min(min(kTile, ti[1].sk - c1 * kTile), vl1);
                     items[ks] = it;
                     mbar_arrive_expect_tx(bar(C::bKF + ks), C::kTileBytes);
                     for (int x = 0; x < C::kSub; ++x)
@@ -331,6 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     end.krow = 0;
                     end.n0 = end.n1 = -1;
                     end.flags = kEnd;
+                    end.lim0 = end.lim1 = 0;
+                    end.pad0 = end.pad1 = 0;
                     items[ks] = end;
                     mbar_arrive(bar(C::bKF + ks));
                     ++kc;
@@ -354,6 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+            // Descriptors are built once; per K step only the 16-byte-unit start
+            // address moves (every operand address is below 2^18, so the 14-bit
+            // address field never carries into the neighbouring fields).
+            const uint64_t desc_q = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t desc_k = smem_desc_sw128(sK, 16, 1024);
+            const uint64_t desc_v = smem_desc_sw128(sV, kSubTileBytes, 1024);
+            constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
+            constexpr uint64_t kSubUnits = kSubTileBytes >> 4;
             uint32_t kc = 0, vc = 0, uc = 0;
             uint32_t pc[2] = {0, 0};
             for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
@@ -363,29 +388,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 // O_t += P_t V for the tile's pending item.
                 auto issue_pv = [&](int t) -> bool {
-                    if (!mbar_wait(bar(C::bPR + t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                    // P_t arrives in two halves of 64 keys; the first four K steps go
+                    // out as soon as the first half is in TMEM.
+                    // Each half has its own barrier, completed once per item: a single
+                    // barrier signalled twice could run two phases ahead of this wait.
+                    if (!mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
                         return false;
-                    ++pc[t];
                     const uint32_t vcx = (uint32_t)pend[t];
                     const uint32_t vs = vcx % C::kStagesV;
                     if (!mbar_wait(bar(C::bVF + vs), (vcx / C::kStagesV) & 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
                         return false;
                     tc_fence_after();
-                    const uint32_t vbase = sV + vs * C::kTileBytes;
+                    const uint64_t vdesc = desc_v + vs * kTileUnits;
+                    const uint32_t o_tmem = tmem + 256 + t * D, p_tmem = tmem + t * 128;
+                    const uint32_t acc0 = first_pv[t] ? 0u : 1u;
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
-                        const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, kSubTileBytes, 1024);
-                        mma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-                               (kk > 0 || !first_pv[t]) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kTile / 32; ++kk)
+                        mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                               kk > 0 ? 1u : acc0);
+                    if (!mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT))
+                        return false;
+                    ++pc[t];
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = kTile / 32; kk < kTile / 16; ++kk)
+                        mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
                     first_pv[t] = false;
-                    mma_commit(bar(C::bOD + t));
                     if (pend[1 - t] != pend[t]) mma_commit(bar(C::bVE + vs));
                     pend[t] = -1;
                     return true;
                 };
                 while (ok) {
+                    // Tile 0's pending P.V needs no K tile, only its P and V: issue it
+                    // before waiting for the next K tile.
+                    if (kPvBeforeK && pend[0] >= 0 && !(ok = issue_pv(0))) break;
                     const uint32_t ks = kc % C::kStagesK;
                     if (!mbar_wait(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT)) {
@@ -399,10 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.n0 = vi->n0;
                         it.n1 = vi->n1;
                         it.flags = vi->flags;
+                        it.lim0 = vi->lim0;
+                        it.lim1 = vi->lim1;
                     }
                     if (it.flags & kEnd) {
-                        for (int t = 0; t < 2 && ok; ++t)
-                            if (pend[t] >= 0) ok = issue_pv(t);
+                        if (pend[0] >= 0 && !(ok = issue_pv(0))) break;
+                        if (pend[1] >= 0 && !(ok = issue_pv(1))) break;
                         for (int t = 0; t < 2 && ok; ++t)
                             if (!have_q[t])
                                 ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
@@ -430,15 +470,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             have_q[t] = true;
                             tc_fence_after();
                         }
-                        const uint32_t qbase = sQ + t * C::kTileBytes;
-                        const uint32_t kbase = sK + ks * C::kTileBytes;
+                        const uint64_t qd = desc_q + t * kTileUnits;
+                        const uint64_t kd = desc_k + ks * kTileUnits;
+                        const uint32_t s_tmem = tmem + t * 128;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kSubTileBytes + (kk & 3) * 32;
-                            mma_ss(tmem + t * 128, smem_desc_sw128(qbase + off, 16, 1024),
-                                   smem_desc_sw128(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                            const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
+                            mma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                         }
                         sinfo[t].n = t ? it.n1 : it.n0;
+                        sinfo[t].lim = t ? it.lim1 : it.lim0;
                         sinfo[t].flags = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
                                          ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
                         mma_commit(bar(C::bSR + t));
@@ -446,8 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pend[t] = (int)vc;
                     }
                     if (!ok) break;
-                    // A tile that sits this item out retires its pending P.V now, so a
-                    // V stage is never held across more than one item.
+                    // Tile 1 retires a pending P.V at once if it sits this item out, so a
+                    // V stage is never held across more than one item (tile 0 already
+                    // issued its pending P.V above).
                     for (int t = 0; t < 2 && ok; ++t)
                         if (!(it.flags & (t ? kPart1 : kPart0)) && pend[t] >= 0) ok = issue_pv(t);
                     if (!ok) break;
@@ -471,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_col = (uint32_t)t * 128u;
         const uint32_t o_col = 256u + (uint32_t)t * D;
         const float sl2 = p.scale_log2;
-        uint32_t scount = 0, pvcount = 0;
+        uint32_t scount = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const int h = u / p.pairs_per_head;
             const int pr = u - h * p.pairs_per_head;
@@ -491,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const volatile SInfo *vs = &sinfo[t];
                     si.n = vs->n;
                     si.flags = vs->flags;
+                    si.lim = vs->lim;
                 }
                 if (si.flags & kSEnd) break;
 
@@ -515,59 +558,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (si.flags & (kSMask | kSBound)) {
-                    // Keep-mask of the 128 columns as four 32-bit words, then one pass
-                    // that sets the dropped scores to -inf.
+                    // Keep-mask of the 128 columns as four 32-bit words; columns at or
+                    // past si.lim (sequence end, valid length) are always dropped.
                     const int j0 = si.n * kTile;
-                    int lim = min(kTile, ti.sk - j0);  // keys inside the sequence
+                    const int lim = si.lim;
                     uint32_t keep[4];
-                    if (!(si.flags & kSMask)) {
+                    if (!(si.flags & kSMask) || p.kind == BSATTN_MASK_NONE) {
 #pragma unroll
                         for (int w = 0; w < 4; ++w) keep[w] = span_bits(0, lim - 32 * w);
-                    } else {
-                        if (p.vl) lim = min(lim, __ldg(p.vl + (long long)ti.b * p.vl_stride + si.n));
-                        if (p.kind == BSATTN_MASK_DOCUMENT) {
-                            const int32_t dq = __ldg(p.doc_q + ti.qrow0 + min(r, ti.nvalid - 1));
-                            const int32_t *dk = p.doc_k + (long long)ti.krow0 + j0;
+                    } else if (p.kind == BSATTN_MASK_DOCUMENT) {
+                        const int32_t dq = __ldg(p.doc_q + ti.qrow0 + min(r, ti.nvalid - 1));
+                        const int32_t *dk = p.doc_k + (long long)ti.krow0 + j0;
 #pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                uint32_t bits = 0;
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t bits = 0;
 #pragma unroll 1
-                                for (int x = 0; x < 32; ++x) {
-                                    const int c = 32 * w + x;
-                                    if (c < lim && __ldg(dk + c) == dq) bits |= 1u << x;
-                                }
-                                keep[w] = bits;
+                            for (int x = 0; x < 32; ++x) {
+                                const int c = 32 * w + x;
+                                if (c < lim && __ldg(dk + c) == dq) bits |= 1u << x;
                             }
-                        } else {
-                            const int diag = i_seq - j0 + 1;  // columns c < diag have j <= i
-                            int la = 0, ha = lim, hb = 0;
-                            if (p.kind == BSATTN_MASK_CAUSAL) {
-                                ha = min(lim, diag);
-                            } else if (p.kind == BSATTN_MASK_SLIDING_WINDOW) {
-                                la = diag <= p.window_left ? 0 : diag - p.window_left;
-                                ha = min(lim, diag);
-                                hb = min(ha, p.sink_tokens - j0);
-                            } else if (p.kind == BSATTN_MASK_PREFIX) {
-                                ha = min(lim, max(p.prefix_len - j0, diag));
-                            }
-#pragma unroll
-                            for (int w = 0; w < 4; ++w)
-                                keep[w] = span_bits(la - 32 * w, ha - 32 * w) | span_bits(0, hb - 32 * w);
+                            keep[w] = bits;
                         }
+                    } else {
+                        const int diag = i_seq - j0 + 1;  // columns c < diag have j <= i
+                        int la = 0, ha = lim, hb = 0;
+                        if (p.kind == BSATTN_MASK_CAUSAL) {
+                            ha = min(lim, diag);
+                        } else if (p.kind == BSATTN_MASK_SLIDING_WINDOW) {
+                            la = diag <= p.window_left ? 0 : diag - p.window_left;
+                            ha = min(lim, diag);
+                            hb = min(ha, p.sink_tokens - j0);
+                        } else if (p.kind == BSATTN_MASK_PREFIX) {
+                            ha = min(lim, max(p.prefix_len - j0, diag));
+                        }
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            keep[w] = span_bits(la - 32 * w, ha - 32 * w) | span_bits(0, hb - 32 * w);
                     }
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (!((keep[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                    for (int w = 0; w < 4; ++w) {
+                        if (keep[w] == 0xffffffffu) continue;
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                        for (int x = 0; x < 32; ++x)
+                            if (!((keep[w] >> x) & 1u)) s[32 * w + x] = -INFINITY;
+                    }
                 }
-                const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+                float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+                for (int c = 12; c < 124; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+                }
+                mx0 = fmax3(mx0, s[124], s[125]);
+                mx1 = fmax3(mx1, s[126], s[127]);
+                const float m_new = fmaxf(m_run, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
                 // Rescale O only when some row's running maximum grew by more than 2^8;
                 // otherwise keep the stale maximum (O / l at the end is the same).
                 const bool rescale = (j > 0) && __any_sync(0xffffffffu, (m_new - m_run) > 8.0f);
@@ -576,29 +623,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (rescale && m_new != -INFINITY) alpha = ex2_approx(m_run - m_new);
                     m_run = m_new;
                 }
-                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
+                float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
+                auto p_half = [&](int c) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
-                        const float p0 = ex2_approx(fmaf(s[c * 64 + 2 * x], sl2, -m_use));
-                        const float p1 = ex2_approx(fmaf(s[c * 64 + 2 * x + 1], sl2, -m_use));
-                        l0 += p0;
-                        l1 += p1;
+                        float x0, x1;
+                        ffma2(x0, x1, s[c * 64 + 2 * x], s[c * 64 + 2 * x + 1], sl2, sl2, nm, nm);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        if (x & 1) fadd2(lb0, lb1, lb0, lb1, p0, p1);
+                        else fadd2(la0, la1, la0, la1, p0, p1);
                         pk[x] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(lane_addr + s_col + c * 32, pk);
-                }
-                l_run = l_run * alpha + (l0 + l1);
+                };
+                // Publish P to the MMA warp in two halves (keys 0-63, then 64-127).
+                auto publish = [&](int half) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::bPR + 2 * t + half));
+                };
+                p_half(0);
                 if (rescale) {
-                    // O_t must hold the previous item's P.V before it is rescaled.
-                    ok = mbar_wait(bar(C::bOD + t), (pvcount - 1) & 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
+                    // S_t of this item was issued after the previous item's P.V, so
+                    // its completion (observed above) means O_t is up to date.
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
@@ -611,11 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(lane_addr + o_col + c * 32, v);
                     }
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::bPR + t));
-                ++pvcount;
+                publish(0);
+                p_half(1);
+                publish(1);
+                const float l0 = la0 + lb0, l1 = la1 + lb1;
+                l_run = l_run * alpha + (l0 + l1);
                 ++j;
             }
             if (!ok) break;
