@@ -18,11 +18,12 @@ from ._binding import (BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUP
                        MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX, MASK_SLIDING_WINDOW,
                        OUT_BF16, OUT_F32,
                        BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
-                       bsattn_fwd, library, status_string)
+                       bsattn_fwd, bsattn_fwd_workspace_size, library, status_string)
 
 TILE = 128
 
-__all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_abi_version", "alloc_meta", "build_meta",
+__all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_fwd_workspace_size", "bsattn_abi_version",
+           "alloc_meta", "alloc_workspace", "build_meta",
            "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
            "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
            "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA",
@@ -60,6 +61,13 @@ def alloc_meta(B: int, H: int, *, varlen: bool = False, seqlen_q: int = 0, seqle
                 num_n=nn)
 
 
+def alloc_workspace(meta: Meta, device="cuda"):
+    """Scheduling workspace for bsattn_fwd (None when the problem needs none)."""
+    import torch
+    n = bsattn_fwd_workspace_size(meta)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
 def _check(status: int, where: str) -> None:
     if status != BSATTN_OK:
         raise BsattnError(status, where)
@@ -78,11 +86,13 @@ def build_meta(block_map, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, s
 def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_valid_len=None,
             kind: int = MASK_NONE, mask_params: Optional[MaskParams] = None,
             softmax_scale: Optional[float] = None, out=None, out_dtype=None, lse=None,
-            err_flag=None, stream=None):
+            workspace="auto", err_flag=None, stream=None):
     """Block-sparse attention forward.  q/k/v: bf16 [B, S, H, D] or packed [total, H, D].
 
     Returns (out, lse): out shaped like q (bf16 by default, or torch.float32),
-    lse fp32 [B, H, S_q] (batched) or [H, total_q]."""
+    lse fp32 [B, H, S_q] (batched) or [H, total_q].  workspace: "auto" allocates
+    the scheduling workspace for this call, None uses the fixed-stride schedule,
+    a tensor is used as given (see alloc_workspace)."""
     import torch
     varlen = bool(meta.varlen)
     if varlen:
@@ -105,8 +115,11 @@ def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_val
         raise ValueError("out.dtype and out_dtype disagree")
     if lse is None:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    if isinstance(workspace, str):
+        workspace = alloc_workspace(meta, q.device)
     _check(bsattn_fwd(q, k, v, meta.B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta,
                       kv_valid_len, kind, mask_params, softmax_scale, out,
-                      OUT_F32 if out_dtype == torch.float32 else OUT_BF16, lse, err_flag, stream),
+                      OUT_F32 if out_dtype == torch.float32 else OUT_BF16, lse, workspace=workspace,
+                      err_flag=err_flag, stream=stream),
            "bsattn_fwd")
     return out, lse

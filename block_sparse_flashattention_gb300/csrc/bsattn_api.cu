@@ -11,6 +11,9 @@ namespace {
 
 using bsattn::kTile;
 
+// Workspace: the claim counter in the first 256 bytes, then the unit order.
+constexpr size_t kWorkspaceHeader = 256;
+
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -112,6 +115,19 @@ const char *bsattn_status_string(bsattn_status s) {
 
 int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
 
+bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
+    if (!bytes) return BSATTN_ERR_INVALID_ARG;
+    *bytes = 0;
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    const long long total_m =
+        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
+    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
+    *bytes = (size_t)(kWorkspaceHeader + 4 * units);
+    return BSATTN_OK;
+}
+
 bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
                                 const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
                                 const int32_t *kv_valid_len, bsattn_mask_kind kind,
@@ -172,7 +188,8 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
                          const int32_t *cu_seqlens_k, const bsattn_meta *meta,
                          const int32_t *kv_valid_len, bsattn_mask_kind kind,
                          const bsattn_mask_params *mp, float softmax_scale, void *out,
-                         bsattn_out_dtype out_dtype, float *lse, int32_t *err_flag, void *stream) {
+                         bsattn_out_dtype out_dtype, float *lse, void *workspace,
+                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
@@ -239,6 +256,17 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
     if ((long long)H * p.pairs_per_head > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
     p.num_units = H * p.pairs_per_head;
     if (p.num_units == 0 || rows_q == 0) return BSATTN_OK;
+    if (workspace) {
+        if (!aligned16(workspace)) return BSATTN_ERR_INVALID_ARG;
+        size_t need = 0;
+        if ((st = bsattn_fwd_workspace_size(meta, &need)) != BSATTN_OK) return st;
+        if (need > 0) {
+            if (workspace_bytes < need) return BSATTN_ERR_INVALID_ARG;
+            p.dynamic = 1;
+            p.sched_counter = static_cast<uint32_t *>(workspace);
+            p.sched_order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kWorkspaceHeader);
+        }
+    }
 
     CUtensorMap tq, tk, tv;
     if (!encode_bshd(&tq, q, rows_q, H, D) || !encode_bshd(&tk, k, rows_k > 0 ? rows_k : 1, H, D) ||

@@ -35,21 +35,22 @@ constexpr uint32_t kTmemCols = 512;
 // Register split: the kernel is built for 168 registers per thread at launch
 // (65536 / 384, rounded down to a multiple of 8), i.e. 64512 for the CTA.  The
 // control warpgroup gives registers back and the two softmax warpgroups take
-// them: 128 * 88 + 2 * 128 * 208 = 64512, exactly the launch allocation.
+// them: 128 * 120 + 2 * 128 * 192 = 64512, exactly the launch allocation.
+// (setmaxnreg sits inside each role's branch so that ptxas applies the budget there.)
 constexpr int kLaunchRegs = 168;
 constexpr int kStagesK128 = 2;  // K ring depth at d = 128 (3 measured no faster)
-// Issue tile 0's pending P.V before waiting for the next K tile (measured no faster).
-constexpr bool kPvBeforeK = false;
-constexpr uint32_t kCtrlRegs = 88, kSoftmaxRegs = 208;
+constexpr uint32_t kCtrlRegs = 120, kSoftmaxRegs = 192;
 static_assert(128 * kCtrlRegs + 2 * 128 * kSoftmaxRegs <= (uint32_t)kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kSubTileBytes = kTile * 64 * 2;  // 128 rows x 64 bf16 (one 128-byte swizzle span)
 
 // Item flags (producer -> MMA issuer).
 constexpr uint32_t kPart0 = 1u, kPart1 = 2u, kMask0 = 4u, kMask1 = 8u, kEnd = 16u, kBound0 = 32u,
-                   kBound1 = 64u;
+                   kBound1 = 64u, kLast0 = 128u, kLast1 = 256u,  // kLast_t: tile t's last item
+                   kStop = 512u;                                  // no further units
 // Per-tile flags (MMA issuer -> softmax).
-constexpr uint32_t kSMask = 1u, kSBound = 2u, kSEnd = 4u;
+constexpr uint32_t kSMask = 1u, kSBound = 2u, kSEnd = 4u, kSStop = 8u;
+constexpr int kUnitRing = 4;  // unit ids in flight between the producer and the softmax
 
 struct Item {
     int32_t krow;  // packed K/V row of the tile
@@ -67,6 +68,32 @@ struct SInfo {
     int32_t pad;
 };
 
+struct TileInfo {
+    int valid;
+    int b, m;
+    int qrow0;    // packed q row of the tile's first row
+    int nvalid;   // rows of the tile inside the sequence
+    int krow0;    // packed k row of the sequence's first key
+    int sk;       // seqlen_k(b)
+    int nn;       // num_n(b)
+    long long cnt_at, idx_at;
+};
+
+// What the scheduler warp hands the producer for one unit: the unit id, where
+// its two Q tiles sit, and the head of each of their lists (counts, first two
+// entries, and the valid length of the first mask tile), so that the producer
+// can issue the unit's first loads without waiting on global memory.
+struct UnitDesc {
+    TileInfo ti[2];
+    int32_t u;       // unit id; -1: no further units
+    int32_t cnt[4];  // [2t] mask count, [2t + 1] full count of tile t, as stored
+    int32_t e0[4];   // first entry of each list (-1 if the list has no room for it)
+    int32_t e1[4];   // second entry
+    int32_t vl[2];   // valid length of tile t's first mask entry (kTile without one)
+    int32_t pad;
+};
+constexpr int kUnitDescs = 2;
+
 template <int D>
 struct Cfg {
     static constexpr int kStagesK = D == 128 ? kStagesK128 : 4;
@@ -80,24 +107,20 @@ struct Cfg {
     // barrier indices
     static constexpr int bKF = 0, bKE = kStagesK, bVF = 2 * kStagesK, bVE = 2 * kStagesK + kStagesV;
     static constexpr int bQF = 2 * kStagesK + 2 * kStagesV, bQE = bQF + 2, bSR = bQF + 4,
-                         bPR = bQF + 6, bDrain = bQF + 10, kNumBars = bQF + 11;  // bPR + 2t + half
+                         bPR = bQF + 6,  // bPR + 2t + half
+                         bED = bQF + 10, bUF = bQF + 12, bUE = bQF + 14, bDrain = bQF + 16,
+                         kNumBars = bQF + 17;
     static constexpr uint32_t kItems = kBar + kNumBars * 8;
     static constexpr uint32_t kSInfo = kItems + kStagesK * sizeof(Item);
-    static constexpr uint32_t kMisc = kSInfo + 2 * sizeof(SInfo);  // [0] tmem base, [1] abort
-    static constexpr uint32_t kBytes = kMisc + 16;
+    static constexpr uint32_t kUnits = kSInfo + 2 * sizeof(SInfo);
+    static constexpr uint32_t kMisc = kUnits + kUnitRing * 4;  // [0] tmem base, [1] abort
+    static constexpr uint32_t kUDesc = kMisc + 16;               // 2 unit descriptors
+    // Epilogue scratch: 4 KB per softmax warp (32 rows x 128 bytes).
+    static constexpr uint32_t kEpi = (kUDesc + kUnitDescs * sizeof(UnitDesc) + 127u) & ~127u;
+    static constexpr uint32_t kBytes = kEpi + 8u * 4096u;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-struct TileInfo {
-    int valid;
-    int b, m;
-    int qrow0;    // packed q row of the tile's first row
-    int nvalid;   // rows of the tile inside the sequence
-    int krow0;    // packed k row of the sequence's first key
-    int sk;       // seqlen_k(b)
-    int nn;       // num_n(b)
-    long long cnt_at, idx_at;
-};
 
 __device__ __forceinline__ TileInfo tile_info(const FwdParams &p, int h, int T) {
     TileInfo t;
@@ -171,16 +194,25 @@ __device__ __forceinline__ void cur_advance(Cursor &c, int nn, int32_t *err) {
     }
 }
 
-__device__ __forceinline__ void cur_init(Cursor &c, const int32_t *ptr, int cnt, int nn,
-                                         int32_t *err) {
+// Starts a cursor on a list whose count and first two entries were read ahead
+// (e1 is only used when the list has two entries).
+__device__ __forceinline__ void cur_init(Cursor &c, const int32_t *ptr, int cnt, int e0, int e1,
+                                         int nn, int32_t *err) {
     if (cnt < 0 || cnt > nn) {
         if (err) atomicOr(err, BSATTN_FLAG_BAD_COUNT);
         cnt = cnt < 0 ? 0 : nn;
     }
     c.ptr = ptr;
     c.cnt = cnt;
-    c.pos = -1;
-    c.pre = cnt > 0 ? __ldg(ptr) : -1;
+    c.pos = 0;
+    if (cnt == 0) {
+        c.head = -1;
+        return;
+    }
+    c.head = e0;
+    c.pre = cnt > 1 ? e1 : -1;
+    if (c.head >= 0 && c.head < nn) return;
+    if (err) atomicOr(err, BSATTN_FLAG_BAD_INDEX);
     cur_advance(c, nn, err);
 }
 
@@ -196,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gbase = smem_raw + (base - raw);
     Item *items = reinterpret_cast<Item *>(gbase + C::kItems);
     SInfo *sinfo = reinterpret_cast<SInfo *>(gbase + C::kSInfo);
+    int32_t *unit_ring = reinterpret_cast<int32_t *>(gbase + C::kUnits);
+    UnitDesc *udesc = reinterpret_cast<UnitDesc *>(gbase + C::kUDesc);
     uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + C::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
     auto bar = [&](int i) -> uint32_t { return base + C::kBar + 8u * (uint32_t)i; };
@@ -219,6 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::bSR + t), 2);
             mbar_init(bar(C::bPR + 2 * t), 4);      // first half of P_t: one arrival per warp
             mbar_init(bar(C::bPR + 2 * t + 1), 4);  // second half
+            mbar_init(bar(C::bED + t), 4);          // softmax t has seen the end of a unit
+        }
+        for (int s = 0; s < kUnitDescs; ++s) {
+            mbar_init(bar(C::bUF + s), 1);  // unit descriptor written (scheduler warp)
+            mbar_init(bar(C::bUE + s), 1);  // unit descriptor taken (producer)
         }
         mbar_init(bar(C::bDrain), 1);
         misc[1] = 0;
@@ -234,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp < 4) regs_release<kCtrlRegs>();
     if (warp == 0) {
+        regs_release<kCtrlRegs>();
         // ------------------------------------------------------- producer --
         if (lane == 0) {
             tma_prefetch_desc(&tq);
@@ -245,10 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // counts the uses of each Q stage.  The drain below derives from them the
             // last phase of every full barrier.
             uint32_t kc = 0, vc = 0, uc = 0, qn0 = 0, qn1 = 0;
-            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+            for (uint32_t un = 0;; ++un) {
+                // The next unit, prepared by the scheduler warp.
+                const uint32_t slot = un % kUnitDescs;
+                if (!mbar_wait(bar(C::bUF + slot), (un / kUnitDescs) & 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT))
+                    goto producer_done;
+                const UnitDesc d = udesc[slot];
+                mbar_arrive(bar(C::bUE + slot));
+                const int u = d.u;
+                if (u < 0) break;
+                unit_ring[uc % kUnitRing] = u;
                 const int h = u / p.pairs_per_head;
-                const int pr = u - h * p.pairs_per_head;
-                TileInfo ti[2] = {tile_info(p, h, 2 * pr), tile_info(p, h, 2 * pr + 1)};
+                const TileInfo ti[2] = {d.ti[0], d.ti[1]};
                 for (int t = 0; t < 2; ++t) {
                     if (!mbar_wait(bar(C::bQE + t), (uc & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
@@ -267,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Cursor cm[2], cf[2];
                 for (int t = 0; t < 2; ++t) {
                     if (ti[t].valid) {
-                        cur_init(cm[t], p.mask_idx + ti[t].idx_at, __ldg(p.mask_cnt + ti[t].cnt_at),
-                                 ti[t].nn, p.err);
-                        cur_init(cf[t], p.full_idx + ti[t].idx_at, __ldg(p.full_cnt + ti[t].cnt_at),
-                                 ti[t].nn, p.err);
+                        cur_init(cm[t], p.mask_idx + ti[t].idx_at, d.cnt[2 * t], d.e0[2 * t],
+                                 d.e1[2 * t], ti[t].nn, p.err);
+                        cur_init(cf[t], p.full_idx + ti[t].idx_at, d.cnt[2 * t + 1], d.e0[2 * t + 1],
+                                 d.e1[2 * t + 1], ti[t].nn, p.err);
                     } else {
                         cm[t].head = cf[t].head = -1;
                         cm[t].cnt = cf[t].cnt = 0;
@@ -297,7 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.flags |= kPart0;
                         if (cm[0].head == c0) {
                             it.flags |= kMask0;
-                            if (p.vl) vl0 = __ldg(p.vl + (long long)ti[0].b * p.vl_stride + c0);
+                            if (p.vl)
+                                vl0 = cm[0].pos == 0 ? d.vl[0]
+                                                     : __ldg(p.vl + (long long)ti[0].b * p.vl_stride + c0);
                             cur_advance(cm[0], ti[0].nn, p.err);
                         } else {
                             cur_advance(cf[0], ti[0].nn, p.err);
@@ -308,13 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.flags |= kPart1;
                         if (cm[1].head == c1) {
                             it.flags |= kMask1;
-                            if (p.vl) vl1 = __ldg(p.vl + (long long)ti[1].b * p.vl_stride + c1);
+                            if (p.vl)
+                                vl1 = cm[1].pos == 0 ? d.vl[1]
+                                                     : __ldg(p.vl + (long long)ti[1].b * p.vl_stride + c1);
                             cur_advance(cm[1], ti[1].nn, p.err);
                         } else {
                             cur_advance(cf[1], ti[1].nn, p.err);
                         }
                         if ((c1 + 1) * kTile > ti[1].sk) it.flags |= kBound1;
                     }
+                    // A tile whose lists are now exhausted is done with its Q tile after
+                    // this item's S: the MMA warp releases that Q buffer early.
+                    if (p0 && max(cm[0].head, cf[0].head) < 0) it.flags |= kLast0;
+                    if (p1 && max(cm[1].head, cf[1].head) < 0) it.flags |= kLast1;
                     const uint32_t ks = kc % C::kStagesK;
                     if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
@@ -352,6 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bar(C::bKF + ks));
                     ++kc;
                 }
+                ++uc;
+            }
+            {
+                const uint32_t ks = kc % C::kStagesK;
+                if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT))
+                    goto producer_done;
+                Item stop;
+                stop.krow = 0;
+                stop.n0 = stop.n1 = -1;
+                stop.flags = kStop;
+                stop.lim0 = stop.lim1 = 0;
+                stop.pad0 = stop.pad1 = 0;
+                items[ks] = stop;
+                mbar_arrive(bar(C::bKF + ks));
+                ++kc;
             }
         producer_done:
             // Make sure no TMA write into this CTA's shared memory is still in flight.
@@ -367,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qn1 > 0) mbar_wait_drain(bar(C::bQF + 1), (qn1 - 1) & 1u);
         }
     } else if (warp == 1) {
+        regs_release<kCtrlRegs>();
         // ---------------------------------------------------- MMA issuer --
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
@@ -380,129 +453,224 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t kTileUnits = C::kTileBytes >> 4;
             constexpr uint64_t kSubUnits = kSubTileBytes >> 4;
             uint32_t kc = 0, vc = 0, uc = 0;
-            uint32_t pc[2] = {0, 0};
-            for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
-                bool have_q[2] = {false, false};
-                bool first_pv[2] = {true, true};
-                int pend[2] = {-1, -1};  // V-ring item counter of the tile's pending P.V
-                bool ok = true;
-                // O_t += P_t V for the tile's pending item.
-                auto issue_pv = [&](int t) -> bool {
-                    // P_t arrives in two halves of 64 keys; the first four K steps go
-                    // out as soon as the first half is in TMEM.
-                    // Each half has its own barrier, completed once per item: a single
-                    // barrier signalled twice could run two phases ahead of this wait.
-                    if (!mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
-                        return false;
-                    const uint32_t vcx = (uint32_t)pend[t];
-                    const uint32_t vs = vcx % C::kStagesV;
-                    if (!mbar_wait(bar(C::bVF + vs), (vcx / C::kStagesV) & 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
-                        return false;
-                    tc_fence_after();
-                    const uint64_t vdesc = desc_v + vs * kTileUnits;
-                    const uint32_t o_tmem = tmem + 256 + t * D, p_tmem = tmem + t * 128;
-                    const uint32_t acc0 = first_pv[t] ? 0u : 1u;
+            uint32_t pc[2] = {0, 0}, edc[2] = {0, 0};
+            bool need_ed[2] = {false, false};
+            // per-unit state
+            bool have_q[2] = {false, false};
+            bool q_released[2] = {false, false};
+            bool first_pv[2] = {true, true};
+            int pend[2] = {-1, -1};  // V-ring item counter of the tile's pending P.V
+            bool ok = true;
+            // O_t += P_t V for the tile's pending item.  P_t arrives in two halves of
+            // 64 keys, each with its own barrier (one barrier signalled twice per item
+            // could run two phases ahead of this wait); the first four K steps go out
+            // as soon as the first half is in TMEM.
+            auto issue_pv = [&](int t) -> bool {
+                if (!mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                    return false;
+                const uint32_t vcx = (uint32_t)pend[t];
+                const uint32_t vs = vcx % C::kStagesV;
+                if (!mbar_wait(bar(C::bVF + vs), (vcx / C::kStagesV) & 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT))
+                    return false;
+                tc_fence_after();
+                const uint64_t vdesc = desc_v + vs * kTileUnits;
+                const uint32_t o_tmem = tmem + 256 + t * D, p_tmem = tmem + t * 128;
+                const uint32_t acc0 = first_pv[t] ? 0u : 1u;
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 32; ++kk)
-                        mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
-                               kk > 0 ? 1u : acc0);
-                    if (!mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
+                for (int kk = 0; kk < kTile / 32; ++kk)
+                    mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                           kk > 0 ? 1u : acc0);
+                if (!mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT))
+                    return false;
+                ++pc[t];
+                tc_fence_after();
+#pragma unroll
+                for (int kk = kTile / 32; kk < kTile / 16; ++kk)
+                    mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
+                first_pv[t] = false;
+                if (pend[1 - t] != pend[t]) mma_commit(bar(C::bVE + vs));
+                pend[t] = -1;
+                return true;
+            };
+            // Publishes sinfo[t] and signals tile t's S-ready barrier.  After an end
+            // of unit, the softmax must first acknowledge that end: the barrier could
+            // otherwise complete two phases before the softmax waits on it.
+            auto signal_s = [&](int t, int32_t n, int32_t lim, uint32_t fl) -> bool {
+                if (need_ed[t]) {
+                    if (!mbar_wait(bar(C::bED + t), edc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
                         return false;
-                    ++pc[t];
-                    tc_fence_after();
+                    ++edc[t];
+                    need_ed[t] = false;
+                }
+                sinfo[t].n = n;
+                sinfo[t].lim = lim;
+                sinfo[t].flags = fl;
+                mma_commit(bar(C::bSR + t));
+                mbar_arrive(bar(C::bSR + t));
+                return true;
+            };
+            while (ok) {
+                const uint32_t ks = kc % C::kStagesK;
+                if (!(ok = mbar_wait(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
+                                     BSATTN_FLAG_TIMEOUT)))
+                    break;
+                Item it;
+                {
+                    const volatile Item *vi = &items[ks];
+                    it.krow = vi->krow;
+                    it.n0 = vi->n0;
+                    it.n1 = vi->n1;
+                    it.flags = vi->flags;
+                    it.lim0 = vi->lim0;
+                    it.lim1 = vi->lim1;
+                }
+                if (it.flags & kStop) {
+                    
 #pragma unroll
-                    for (int kk = kTile / 32; kk < kTile / 16; ++kk)
-                        mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
-                    first_pv[t] = false;
-                    if (pend[1 - t] != pend[t]) mma_commit(bar(C::bVE + vs));
-                    pend[t] = -1;
-                    return true;
-                };
-                while (ok) {
-                    // Tile 0's pending P.V needs no K tile, only its P and V: issue it
-                    // before waiting for the next K tile.
-                    if (kPvBeforeK && pend[0] >= 0 && !(ok = issue_pv(0))) break;
-                    const uint32_t ks = kc % C::kStagesK;
-                    if (!mbar_wait(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT)) {
-                        ok = false;
-                        break;
-                    }
-                    Item it;
-                    {
-                        const volatile Item *vi = &items[ks];
-                        it.krow = vi->krow;
-                        it.n0 = vi->n0;
-                        it.n1 = vi->n1;
-                        it.flags = vi->flags;
-                        it.lim0 = vi->lim0;
-                        it.lim1 = vi->lim1;
-                    }
-                    if (it.flags & kEnd) {
-                        if (pend[0] >= 0 && !(ok = issue_pv(0))) break;
-                        if (pend[1] >= 0 && !(ok = issue_pv(1))) break;
-                        for (int t = 0; t < 2 && ok; ++t)
-                            if (!have_q[t])
-                                ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
-                                               BSATTN_FLAG_TIMEOUT);
-                        if (!ok) break;
-                        for (int t = 0; t < 2; ++t) mma_commit(bar(C::bQE + t));
-                        mbar_arrive(bar(C::bKE + ks));
-                        for (int t = 0; t < 2; ++t) {
-                            sinfo[t].n = -1;
-                            sinfo[t].flags = kSEnd;
-                            mma_commit(bar(C::bSR + t));
-                            mbar_arrive(bar(C::bSR + t));
-                        }
-                        ++kc;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (!(it.flags & (t ? kPart1 : kPart0))) continue;
-                        if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
-                        if (!have_q[t]) {
-                            if (!(ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
-                                                 BSATTN_FLAG_TIMEOUT)))
-                                break;
-                            have_q[t] = true;
-                            tc_fence_after();
-                        }
-                        const uint64_t qd = desc_q + t * kTileUnits;
-                        const uint64_t kd = desc_k + ks * kTileUnits;
-                        const uint32_t s_tmem = tmem + t * 128;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                            mma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        sinfo[t].n = t ? it.n1 : it.n0;
-                        sinfo[t].lim = t ? it.lim1 : it.lim0;
-                        sinfo[t].flags = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
-                                         ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
-                        mma_commit(bar(C::bSR + t));
-                        mbar_arrive(bar(C::bSR + t));
-                        pend[t] = (int)vc;
-                    }
-                    if (!ok) break;
-                    // Tile 1 retires a pending P.V at once if it sits this item out, so a
-                    // V stage is never held across more than one item (tile 0 already
-                    // issued its pending P.V above).
-                    for (int t = 0; t < 2 && ok; ++t)
-                        if (!(it.flags & (t ? kPart1 : kPart0)) && pend[t] >= 0) ok = issue_pv(t);
-                    if (!ok) break;
-                    mma_commit(bar(C::bKE + ks));
+                    for (int t = 0; t < 2; ++t)
+                        if (ok) ok = signal_s(t, -1, 0, kSStop);
                     ++kc;
-                    ++vc;
+                    break;
+                }
+                if (it.flags & kEnd) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (ok && pend[t] >= 0) ok = issue_pv(t);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (ok && !have_q[t])
+                            ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                           BSATTN_FLAG_TIMEOUT);
+                    if (!ok) break;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (!q_released[t]) mma_commit(bar(C::bQE + t));
+                    mbar_arrive(bar(C::bKE + ks));
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (ok) ok = signal_s(t, -1, 0, kSEnd);
+                        need_ed[t] = true;
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        have_q[t] = q_released[t] = false;
+                        first_pv[t] = true;
+                        pend[t] = -1;
+                    }
+                    ++uc;
+                    ++kc;
+                    continue;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok) break;
+                    if (!(it.flags & (t ? kPart1 : kPart0))) continue;
+                    if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
+                    if (!have_q[t]) {
+                        if (!(ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                             BSATTN_FLAG_TIMEOUT)))
+                            break;
+                        have_q[t] = true;
+                        tc_fence_after();
+                    }
+                    const uint64_t qd = desc_q + t * kTileUnits;
+                    const uint64_t kd = desc_k + ks * kTileUnits;
+                    const uint32_t s_tmem = tmem + t * 128;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
+                        mma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    const uint32_t sfl = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
+                                         ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
+                    if (!(ok = signal_s(t, t ? it.n1 : it.n0, t ? it.lim1 : it.lim0, sfl))) break;
+                    if (it.flags & (t ? kLast1 : kLast0)) {
+                        mma_commit(bar(C::bQE + t));  // no further S_t in this unit
+                        q_released[t] = true;
+                    }
+                    pend[t] = (int)vc;
                 }
                 if (!ok) break;
+                // A tile that sits this item out retires its pending P.V now, so a
+                // V stage is never held across more than one item.
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    if (ok && !(it.flags & (t ? kPart1 : kPart0)) && pend[t] >= 0) ok = issue_pv(t);
+                if (!ok) break;
+                mma_commit(bar(C::bKE + ks));
+                ++kc;
+                ++vc;
             }
             // Wait until every tcgen05 operation issued above has completed.
             mma_commit(bar(C::bDrain));
             mbar_wait_drain(bar(C::bDrain), 0);
         }
+    } else if (warp == 3) {
+        regs_release<kCtrlRegs>();
+        // ------------------------------------------------------ scheduler --
+        // Claims units and reads the head of their lists one unit ahead of the
+        // producer.  Units come either from a fixed stride over the CTAs, or, with a
+        // schedule, from an order array claimed slot by slot through an atomic
+        // counter.
+        if (lane == 0) {
+            int u;
+            if (p.dynamic) {
+                const uint32_t pos = atomicAdd(p.sched_counter, 1u);
+                u = pos < (uint32_t)p.num_units ? __ldg(p.sched_order + pos) : -1;
+            } else {
+                u = (int)blockIdx.x < p.num_units ? (int)blockIdx.x : -1;
+            }
+            for (uint32_t n = 0;; ++n) {
+                const uint32_t slot = n % kUnitDescs;
+                if (!mbar_wait(bar(C::bUE + slot), ((n / kUnitDescs) & 1) ^ 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT))
+                    break;
+                UnitDesc &d = udesc[slot];
+                d.u = u;
+                if (u < 0) {
+                    mbar_arrive(bar(C::bUF + slot));
+                    break;
+                }
+                const uint32_t claim = p.dynamic ? atomicAdd(p.sched_counter, 1u) : 0u;
+                const int h = u / p.pairs_per_head;
+                const int pr = u - h * p.pairs_per_head;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const TileInfo ti = tile_info(p, h, 2 * pr + t);
+                    d.ti[t] = ti;
+                    int cm = 0, cf = 0, m0 = -1, m1 = -1, f0 = -1, f1 = -1, vl = kTile;
+                    if (ti.valid) {
+                        cm = __ldg(p.mask_cnt + ti.cnt_at);
+                        cf = __ldg(p.full_cnt + ti.cnt_at);
+                        m0 = __ldg(p.mask_idx + ti.idx_at);
+                        f0 = __ldg(p.full_idx + ti.idx_at);
+                        if (ti.nn > 1) {
+                            m1 = __ldg(p.mask_idx + ti.idx_at + 1);
+                            f1 = __ldg(p.full_idx + ti.idx_at + 1);
+                        }
+                        if (p.vl && cm > 0 && m0 >= 0 && m0 < ti.nn)
+                            vl = __ldg(p.vl + (long long)ti.b * p.vl_stride + m0);
+                    }
+                    d.cnt[2 * t] = cm;
+                    d.cnt[2 * t + 1] = cf;
+                    d.e0[2 * t] = m0;
+                    d.e0[2 * t + 1] = f0;
+                    d.e1[2 * t] = m1;
+                    d.e1[2 * t + 1] = f1;
+                    d.vl[t] = vl;
+                }
+                mbar_arrive(bar(C::bUF + slot));
+                if (p.dynamic)
+                    u = claim < (uint32_t)p.num_units ? __ldg(p.sched_order + claim) : -1;
+                else
+                    u = (long long)u + gridDim.x < p.num_units ? u + (int)gridDim.x : -1;
+            }
+        }
+    } else if (warp < 4) {
+        regs_release<kCtrlRegs>();  // warp 2: idle until the teardown
     } else if (warp >= 4) {
         // ------------------------------------------------------- softmax --
         regs_claim<kSoftmaxRegs>();
@@ -513,30 +681,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_col = (uint32_t)t * 128u;
         const uint32_t o_col = 256u + (uint32_t)t * D;
         const float sl2 = p.scale_log2;
-        uint32_t scount = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        uint32_t scount = 0, ucs = 0;
+        bool ok = true;
+        SInfo si;
+        // Next event (S tile, end of unit, or stop) for this tile.
+        auto wait_s = [&]() -> bool {
+            bool w = mbar_wait(bar(C::bSR + t), scount & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+            w = __all_sync(0xffffffffu, w);
+            if (!w) return false;
+            ++scount;
+            tc_fence_after();
+            const volatile SInfo *vs = &sinfo[t];
+            si.n = vs->n;
+            si.flags = vs->flags;
+            si.lim = vs->lim;
+            return true;
+        };
+        while (ok) {
+            if (!(ok = wait_s())) break;
+            if (si.flags & kSStop) break;
+            // The producer wrote this unit's id before the events that led here.
+            const int u = *reinterpret_cast<const volatile int32_t *>(&unit_ring[ucs % kUnitRing]);
             const int h = u / p.pairs_per_head;
             const int pr = u - h * p.pairs_per_head;
             const TileInfo ti = tile_info(p, h, 2 * pr + t);
             const int i_seq = ti.m * kTile + r;  // sequence-local query position
             float m_run = -INFINITY, l_run = 0.f;
             int j = 0;
-            bool ok = true;
             while (true) {
-                ok = mbar_wait(bar(C::bSR + t), scount & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                ++scount;
-                tc_fence_after();
-                SInfo si;
-                {
-                    const volatile SInfo *vs = &sinfo[t];
-                    si.n = vs->n;
-                    si.flags = vs->flags;
-                    si.lim = vs->lim;
+                if (si.flags & kSEnd) {
+                    // Acknowledge the end of the unit: the MMA warp may signal again.
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::bED + t));
+                    break;
                 }
-                if (si.flags & kSEnd) break;
-
                 float s[128];
                 {
                     uint32_t v0[32], v1[32], v2[32], v3[32];
@@ -668,48 +846,95 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float l0 = la0 + lb0, l1 = la1 + lb1;
                 l_run = l_run * alpha + (l0 + l1);
                 ++j;
+                if (!(ok = wait_s())) break;
             }
             if (!ok) break;
-            // Epilogue: O / l in bf16 and LSE = ln(sum of exp(scale * s)).
+            // Epilogue: O / l and LSE = ln(sum of exp(scale * s)).  Each lane holds one
+            // row of 128-byte blocks (64 columns in bf16, 32 in fp32).  A block goes
+            // through the warp's shared-memory scratch (16-byte pieces placed at
+            // piece ^ (row & 7), so that neither side conflicts on banks) and comes
+            // back with lane 8g + j holding piece j of rows 8g..8g+7: every store
+            // instruction then writes 4 whole 128-byte row segments.
             const bool row_ok = ti.valid && r < ti.nvalid;
-            const long long orow = ((long long)(ti.qrow0 + r) * p.H + h) * D;  // element offset
             const bool empty = (j == 0) || !(l_run > 0.f);
             const float inv = empty ? 0.f : 1.f / l_run;
+            const int gl = (int)(lane & 7u);
+            const int row0 = (int)(quarter * 32u) + 8 * (int)(lane >> 3);  // first row this lane stores
+            const int nrows = ti.valid ? min(max(ti.nvalid - row0, 0), 8) : 0;
+            // The lane number is re-read here (opaque to the compiler) so that the
+            // scratch addresses below are formed in the epilogue instead of being
+            // hoisted out of the unit loop and held in registers through it.
+            uint32_t ln;
+            asm volatile("mov.u32 %0, %%laneid;" : "=r"(ln));
+            uint4 *scr = reinterpret_cast<uint4 *>(gbase + C::kEpi + (warp - 4u) * 4096u);
+            // Writes this lane's block (row = lane) and reads back the 8 pieces it stores.
+            auto exchange = [&](uint32_t (&w)[32]) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                if (j > 0) {
-                    tmem_ld32(lane_addr + o_col + c * 32, v);
-                    tmem_wait_ld();
-                    reg_fence(v);
-                } else {
+                for (int i = 0; i < 8; ++i)
+                    scr[ln * 8u + ((uint32_t)i ^ (ln & 7u))] =
+                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                __syncwarp();
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) v[x] = 0u;
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 x = scr[(ln >> 3) * 64u + (uint32_t)k * 8u + ((ln & 7u) ^ (uint32_t)k)];
+                    w[4 * k] = x.x;
+                    w[4 * k + 1] = x.y;
+                    w[4 * k + 2] = x.z;
+                    w[4 * k + 3] = x.w;
                 }
-                if (!row_ok) continue;
-                if (p.out_f32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + c * 32);
+                __syncwarp();
+            };
+            const long long row_step = (long long)p.H * D;             // elements between rows
+            const long long out0 = ((long long)(ti.qrow0 + row0) * p.H + h) * D;
+            if (p.out_f32) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv,
-                                              __uint_as_float(v[q4 * 4 + 1]) * inv,
-                                              __uint_as_float(v[q4 * 4 + 2]) * inv,
-                                              __uint_as_float(v[q4 * 4 + 3]) * inv);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + orow + c * 32);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t w[32];
+                    if (j > 0) {
+                        tmem_ld32(lane_addr + o_col + c * 32, w);
+                        tmem_wait_ld();
+                        reg_fence(w);
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv,
-                                          __uint_as_float(v[q4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv,
-                                          __uint_as_float(v[q4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv,
-                                          __uint_as_float(v[q4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv,
-                                          __uint_as_float(v[q4 * 8 + 7]) * inv);
-                        dst[q4] = w;
+                        for (int x = 0; x < 32; ++x) w[x] = 0u;
                     }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(__uint_as_float(w[x]) * inv);
+                    exchange(w);
+                    float *dst = static_cast<float *>(p.out) + out0 + c * 32 + 4 * gl;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (k < nrows)
+                            *reinterpret_cast<uint4 *>(dst + k * row_step) =
+                                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t w[32];
+                    if (j > 0) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t v[32];
+                            tmem_ld32(lane_addr + o_col + c * 64 + hf * 32, v);
+                            tmem_wait_ld();
+                            reg_fence(v);
+#pragma unroll
+                            for (int x = 0; x < 16; ++x)
+                                w[16 * hf + x] = pack_bf16x2(__uint_as_float(v[2 * x]) * inv,
+                                                             __uint_as_float(v[2 * x + 1]) * inv);
+                        }
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) w[x] = 0u;
+                    }
+                    exchange(w);
+                    uint16_t *dst = static_cast<uint16_t *>(p.out) + out0 + c * 64 + 8 * gl;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (k < nrows)
+                            *reinterpret_cast<uint4 *>(dst + k * row_step) =
+                                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
                 }
             }
             if (row_ok) {
@@ -721,6 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[li] = lse;
             }
             tc_fence_before();
+            ++ucs;
         }
     }
 
@@ -729,6 +955,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Work of one Q tile = its listed KV tiles (counts clamped to [0, 2^15)).
+__device__ __forceinline__ int tile_weight(const FwdParams &p, int h, int T) {
+    if (T >= p.total_m) return 0;
+    long long at;
+    if (p.varlen) {
+        at = (long long)h * p.total_m + T;
+    } else {
+        const int b = T / p.num_m, m = T - b * p.num_m;
+        at = ((long long)b * p.H + h) * p.num_m + m;
+    }
+    const int w = max(__ldg(p.full_cnt + at), 0) + max(__ldg(p.mask_cnt + at), 0);
+    return min(w, 32767);
+}
+
+// Scheduling pass (one CTA): orders the work units by decreasing work, stable
+// (units of equal work keep their head-major order, which keeps one head's K/V
+// resident in L2 while the CTAs work on it), and resets the claim counter.
+// Heaviest-first claiming is the longest-processing-time rule for list scheduling.
+constexpr int kSchedBuckets = 1024;
+__global__ void __launch_bounds__(1024, 1) bsattn_schedule_kernel(const __grid_constant__ FwdParams p) {
+    __shared__ int start[kSchedBuckets];
+    extern __shared__ uint16_t key_of[];  // [num_units]: kSchedBuckets - 1 - min(work, 1023)
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kSchedBuckets; b += blockDim.x) start[b] = 0;
+    if (tid == 0) *p.sched_counter = 0u;
+    __syncthreads();
+    for (int u = tid; u < p.num_units; u += blockDim.x) {
+        const int h = u / p.pairs_per_head, pr = u - h * p.pairs_per_head;
+        const int w = tile_weight(p, h, 2 * pr) + tile_weight(p, h, 2 * pr + 1);
+        const int key = kSchedBuckets - 1 - min(w, kSchedBuckets - 1);
+        key_of[u] = (uint16_t)key;
+        atomicAdd(&start[key], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of the key histogram
+        int running = 0;
+        for (int base = 0; base < kSchedBuckets; base += 32) {
+            const int v = start[base + tid];
+            int incl = v;
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, d);
+                if (tid >= d) incl += o;
+            }
+            start[base + tid] = running + incl - v;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        // stable scatter, 32 units at a time in unit order
+        const unsigned lt = (1u << tid) - 1u;
+        for (int base = 0; base < p.num_units; base += 32) {
+            const int u = base + tid;
+            const int key = u < p.num_units ? (int)key_of[u] : 0xFFFF;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            if (u < p.num_units) {
+                p.sched_order[start[key] + __popc(peers & lt)] = u;
+            }
+            __syncwarp();
+            if (u < p.num_units && tid == __ffs(peers) - 1) start[key] += __popc(peers);
+            __syncwarp();
+        }
     }
 }
 
@@ -754,6 +1042,17 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
         attr_set_for_device[dev] = 1;
     }
     if (p.num_units <= 0) return cudaSuccess;
+    if (p.dynamic) {
+        const size_t key_bytes = (size_t)p.num_units * sizeof(uint16_t);
+        if (key_bytes > 48 * 1024) {
+            e = cudaFuncSetAttribute(bsattn_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)key_bytes);
+            if (e != cudaSuccess) return e;
+        }
+        bsattn_schedule_kernel<<<1, 1024, key_bytes, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     bsattn_fwd_kernel<D><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();

@@ -48,7 +48,13 @@ struct FwdParams {
     int lse_row_stride;            // batched: seqlen_q; varlen: total q rows
     int pairs_per_head;            // ceil(total_m / 2)
     int num_units;                 // H * pairs_per_head
+    int dynamic;                   // units claimed from sched_order through sched_counter
+    uint32_t *sched_counter;       // workspace: next slot of sched_order
+    int32_t *sched_order;          // workspace: units, heaviest first
 };
+
+// Units the scheduling pass can order (its per-unit keys live in shared memory).
+constexpr int kMaxScheduledUnits = 98304;
 
 cudaError_t launch_meta(const MetaParams &p, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,

@@ -28,6 +28,7 @@
 #ifndef BSATTN_H
 #define BSATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -152,6 +153,13 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
  * softmax_scale > 0.
  * out           device, same shape as q; element type out_dtype.
  * out_dtype     BSATTN_OUT_BF16 or BSATTN_OUT_F32.
+ * workspace     optional device scratch of at least bsattn_fwd_workspace_size() bytes,
+ *               16-byte aligned, contents need not be initialised.  With it, a
+ *               scheduling pass orders the work units (pairs of Q tiles of one head)
+ *               by decreasing work and the persistent CTAs claim them in that order
+ *               (longest-processing-time list scheduling); without it (NULL), CTAs take
+ *               units by a fixed stride.  Results are identical either way.  Two calls
+ *               that may run concurrently must not share a workspace.
  * lse           device fp32, batched [B, H, seqlen_q], varlen [H, seqlen_q].
  * err_flag      optional device int32 word.
  */
@@ -160,7 +168,15 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
                          const int32_t *cu_seqlens_k, const bsattn_meta *meta,
                          const int32_t *kv_valid_len, bsattn_mask_kind kind,
                          const bsattn_mask_params *mp, float softmax_scale, void *out,
-                         bsattn_out_dtype out_dtype, float *lse, int32_t *err_flag, void *stream);
+                         bsattn_out_dtype out_dtype, float *lse, void *workspace,
+                         size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
+ * bsattn_fwd_workspace_size -- bytes of workspace bsattn_fwd can use for this
+ * metadata (0 when the problem is too large for the scheduling pass, in which
+ * case bsattn_fwd ignores any workspace and uses the fixed stride).
+ */
+bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
 
 /* Human-readable name of a status code (static string). */
 const char *bsattn_status_string(bsattn_status status);

@@ -66,11 +66,13 @@ class DeviceWorkload:
                               seqlen_q=sq, seqlen_k=sk, kv_valid_len=self.vl, kind=self.wl.kind,
                               mask_params=self.mask_params, err_flag=err_flag, stream=stream)
 
-    def forward(self, meta, out=None, lse=None, err_flag=None, stream=None, out_dtype=None):
+    def forward(self, meta, out=None, lse=None, err_flag=None, stream=None, out_dtype=None,
+                workspace="auto"):
         return bsa.forward(self.q, self.k, self.v, meta, cu_seqlens_q=self.cu_q,
                            cu_seqlens_k=self.cu_k, kv_valid_len=self.vl, kind=self.wl.kind,
                            mask_params=self.mask_params, softmax_scale=self.wl.scale, out=out,
-                           out_dtype=out_dtype, lse=lse, err_flag=err_flag, stream=stream)
+                           out_dtype=out_dtype, lse=lse, workspace=workspace, err_flag=err_flag,
+                           stream=stream)
 
 
 def meta_to_numpy(meta) -> dict:

@@ -58,7 +58,7 @@ def _fwd(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, seqlen_q=256, seqlen_k=256, H=2, D=128,
              cu_seqlens_q=None, cu_seqlens_k=None, meta=_meta(), kv_valid_len=None,
              kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, out=FAKE,
-             out_dtype=bsa.OUT_BF16, lse=FAKE,
+             out_dtype=bsa.OUT_BF16, lse=FAKE, workspace=None, workspace_bytes=0,
              err_flag=None, stream=0)
     a.update(kw)
     return bsa.bsattn_fwd(**a)
@@ -81,6 +81,8 @@ INV, UNS = bsa.BSATTN_ERR_INVALID_ARG, bsa.BSATTN_ERR_UNSUPPORTED
     (dict(q=FAKE + 2), INV),                       # not 16-byte aligned
     (dict(out=None), INV),
     (dict(out_dtype=7), INV),
+    (dict(workspace=FAKE + 8, workspace_bytes=1 << 20), INV),   # misaligned workspace
+    (dict(workspace=FAKE, workspace_bytes=16), INV),             # too small
     (dict(lse=None), INV),
     (dict(softmax_scale=0.0), INV),
     (dict(softmax_scale=-1.0), INV),
@@ -112,6 +114,16 @@ def test_fwd_rejects_bad_arguments(kw, expect):
 ])
 def test_build_meta_rejects_bad_arguments(kw, expect):
     assert _bm(**kw) == expect
+
+
+def test_workspace_size():
+    # 2 heads x ceil(2 tiles / 2) = 2 units -> 256-byte header + 2 int32
+    assert bsa.bsattn_fwd_workspace_size(_meta()) == 256 + 4 * 2
+    assert bsa.bsattn_fwd_workspace_size(_meta(B=3, num_m=5)) == 256 + 4 * 2 * 8
+    huge = _meta(H=1000, num_m=1000)
+    assert bsa.bsattn_fwd_workspace_size(huge) == 0          # beyond the scheduling pass
+    with pytest.raises(bsa.BsattnError):
+        bsa.bsattn_fwd_workspace_size(_meta(tile_m=64))
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -241,3 +241,27 @@ def test_fwd_has_no_hidden_stall():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert a.elapsed_time(b) / 5 < 50.0, f"{a.elapsed_time(b) / 5:.1f} ms per launch"
+
+
+@pytest.mark.parametrize("which", ["cfg2", "cfg3", "odd", "varlen_ragged"])
+def test_fwd_schedules_agree_bitwise(which):
+    """The scheduled path (work units claimed heaviest first) and the fixed-stride
+    path compute every unit identically, so their outputs agree bit for bit."""
+    wl = {"cfg2": lambda: make_workload(2), "cfg3": lambda: make_workload(3),
+          "odd": lambda: random_workload(231, B=2, H=3, D=64, seqlens_q=[384, 384]),
+          "varlen_ragged": lambda: random_workload(232, B=5, H=2, D=128,
+                                                    seqlens_q=[1, 300, 129, 1000, 77],
+                                                    varlen=True, density=0.4)}[which]()
+    dw = DeviceWorkload(wl, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    meta = dw.build_meta(err_flag=err)
+    ws = bsa.alloc_workspace(meta)
+    assert ws is not None
+    out_a, lse_a = dw.forward(meta, err_flag=err, workspace=None)
+    out_b, lse_b = dw.forward(meta, err_flag=err, workspace=ws)
+    out_c, lse_c = dw.forward(meta, err_flag=err, workspace=ws)     # workspace reused
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for o, l in ((out_b, lse_b), (out_c, lse_c)):
+        assert torch.equal(out_a.view(torch.int16), o.view(torch.int16))
+        assert torch.equal(lse_a, l)
