@@ -262,11 +262,11 @@ def run_native(args):
                       device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ws = bsa.alloc_workspace(meta, dev)   # scheduling workspace, allocated once
+    sched_ws = bsa.alloc_workspace(meta, dev)   # scheduling workspace, allocated once
 
     def step():
         dw.build_meta(meta, err_flag=err)
-        dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=ws)
+        dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=sched_ws)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -292,7 +292,7 @@ def run_native(args):
         ev[i][0].record(stream)
         dw.build_meta(meta, err_flag=err)
         ev[i][1].record(stream)
-        dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=ws)
+        dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=sched_ws)
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -400,7 +400,7 @@ def run_native(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
-        "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if ws is not None else 0)),
+        "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
