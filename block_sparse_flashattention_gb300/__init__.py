@@ -13,20 +13,21 @@ from __future__ import annotations
 import math
 from typing import Optional
 
-from ._binding import (BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUPPORTED,
-                       BSATTN_OK, FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_BAD_SEQLENS, FLAG_TIMEOUT,
+from ._binding import (BSATTN_ERR_CAPACITY, BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_ARG,
+                       BSATTN_ERR_UNSUPPORTED, BSATTN_OK, BSATTN_STATIC_SCRATCH_UNITS, FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_BAD_SEQLENS, FLAG_TIMEOUT,
                        MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX, MASK_SLIDING_WINDOW,
                        OUT_BF16, OUT_F32,
                        BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
-                       bsattn_fwd, bsattn_fwd_workspace_size, library, status_string)
+                       bsattn_fwd, bsattn_fwd_static_scratch, bsattn_fwd_workspace_size, library,
+                       status_string)
 
 TILE = 128
 
-__all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_fwd_workspace_size", "bsattn_abi_version",
+__all__ = ["bsattn_build_meta", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version",
            "alloc_meta", "alloc_workspace", "build_meta",
            "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
            "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
-           "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA",
+           "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA", "BSATTN_ERR_CAPACITY", "BSATTN_STATIC_SCRATCH_UNITS",
            "FLAG_BAD_COUNT", "FLAG_BAD_INDEX", "FLAG_TIMEOUT", "FLAG_BAD_SEQLENS"]
 
 

@@ -14,6 +14,8 @@ from typing import Optional
 from ._build import LIB
 
 BSATTN_OK, BSATTN_ERR_INVALID_ARG, BSATTN_ERR_UNSUPPORTED, BSATTN_ERR_CUDA = 0, 1, 2, 3
+BSATTN_ERR_CAPACITY = 4
+BSATTN_STATIC_SCRATCH_UNITS = 65536
 MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 0, 1, 2, 3, 4
 OUT_BF16, OUT_F32 = 0, 1
 FLAG_BAD_COUNT, FLAG_BAD_INDEX, FLAG_TIMEOUT, FLAG_BAD_SEQLENS = 0x1, 0x2, 0x4, 0x8
@@ -66,6 +68,9 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_fwd.restype = ctypes.c_int
+        lib.bsattn_fwd_static_scratch.argtypes = lib.bsattn_fwd.argtypes[:18] + [
+            ctypes.c_void_p, ctypes.c_void_p]
+        lib.bsattn_fwd_static_scratch.restype = ctypes.c_int
         lib.bsattn_fwd_workspace_size.argtypes = [ctypes.POINTER(bsattn_meta),
                                                   ctypes.POINTER(ctypes.c_size_t)]
         lib.bsattn_fwd_workspace_size.restype = ctypes.c_int
@@ -166,6 +171,21 @@ def bsattn_fwd(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int, cu
         ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(out),
         int(out_dtype), _ptr(lse), _ptr(workspace), int(workspace_bytes), _ptr(err_flag),
         _stream(stream))
+
+
+def bsattn_fwd_static_scratch(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int,
+                              cu_seqlens_q, cu_seqlens_k, meta: Meta, kv_valid_len, kind: int,
+                              mask_params: Optional[MaskParams], softmax_scale: float, out,
+                              out_dtype: int, lse, err_flag=None, stream=None) -> int:
+    """Forwards to the C function of the same name (bsattn_fwd with the library's
+    fixed scheduling scratch; allocates nothing); returns its status code."""
+    mp = mask_params.to_c() if mask_params is not None else None
+    mt = meta.to_c()
+    return library().bsattn_fwd_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), int(B), int(seqlen_q), int(seqlen_k), int(H), int(D),
+        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), ctypes.byref(mt), _ptr(kv_valid_len), int(kind),
+        ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(out),
+        int(out_dtype), _ptr(lse), _ptr(err_flag), _stream(stream))
 
 
 def bsattn_fwd_workspace_size(meta: Meta) -> int:

@@ -109,6 +109,7 @@ const char *bsattn_status_string(bsattn_status s) {
     case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
     case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
     case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
+    case BSATTN_ERR_CAPACITY: return "BSATTN_ERR_CAPACITY";
     default: return "BSATTN_ERR_UNKNOWN";
     }
 }
@@ -279,3 +280,58 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- fixed scheduling scratch --
+// For callers that cannot allocate device memory at call time (a host program
+// with no device allocator of its own, or a loop that must not call cudaMalloc /
+// cudaFree, the latter being device-synchronising): a scheduling workspace of a
+// fixed size that lives in the library's own device data.  One array per device
+// (a __device__ variable has one instance per device); every call on a device
+// uses it, so overlapping calls would race on it.
+namespace {
+
+constexpr size_t kStaticScratchBytes = kWorkspaceHeader + 4u * (size_t)BSATTN_STATIC_SCRATCH_UNITS;
+static_assert(BSATTN_STATIC_SCRATCH_UNITS <= bsattn::kMaxScheduledUnits,
+              "the fixed scratch must stay within the scheduling pass's limit");
+
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the current device's scratch; resolved once per device, with
+// that device current.
+bsattn_status static_scratch_address(void **addr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return BSATTN_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return BSATTN_OK;
+}
+
+}  // namespace
+
+extern "C" bsattn_status bsattn_fwd_static_scratch(
+    const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q, int32_t seqlen_k,
+    int32_t H, int32_t D, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+    const bsattn_meta *meta, const int32_t *kv_valid_len, bsattn_mask_kind kind,
+    const bsattn_mask_params *mp, float softmax_scale, void *out, bsattn_out_dtype out_dtype,
+    float *lse, int32_t *err_flag, void *stream) {
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    const long long total_m =
+        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
+    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    if (units > BSATTN_STATIC_SCRATCH_UNITS) return BSATTN_ERR_CAPACITY;
+    void *scratch = nullptr;
+    if ((st = static_scratch_address(&scratch)) != BSATTN_OK) return st;
+    return bsattn_fwd(q, k, v, B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta,
+                      kv_valid_len, kind, mp, softmax_scale, out, out_dtype, lse, scratch,
+                      kStaticScratchBytes, err_flag, stream);
+}

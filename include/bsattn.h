@@ -41,7 +41,9 @@ typedef enum {
     BSATTN_OK = 0,
     BSATTN_ERR_INVALID_ARG = 1, /* a pointer, size or layout argument is invalid     */
     BSATTN_ERR_UNSUPPORTED = 2, /* valid, but not served by this build (e.g. D=96)   */
-    BSATTN_ERR_CUDA = 3         /* a CUDA call or a kernel launch failed             */
+    BSATTN_ERR_CUDA = 3,        /* a CUDA call or a kernel launch failed             */
+    BSATTN_ERR_CAPACITY = 4     /* the problem exceeds a fixed capacity: see
+                                   bsattn_fwd_static_scratch                         */
 } bsattn_status;
 
 /* Token-level mask_mod applied on mask-list blocks.  Positions are
@@ -177,6 +179,39 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
  * case bsattn_fwd ignores any workspace and uses the fixed stride).
  */
 bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
+
+/*
+ * bsattn_fwd_static_scratch -- bsattn_fwd with the scheduling workspace taken
+ * from a fixed scratch array inside the library, for callers that cannot
+ * allocate device memory at call time: a C or C++ host program that has no
+ * device allocator of its own to hand a workspace from, or a latency-critical
+ * loop that must not call cudaMalloc / cudaFree (cudaFree synchronises the
+ * device).  This call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).  It is an engineering addition: the pages describe no
+ * counterpart.
+ *
+ * Arguments are those of bsattn_fwd without workspace / workspace_bytes, with
+ * the same meaning, layout, ownership and results.
+ *
+ * Capacity: problems of up to BSATTN_STATIC_SCRATCH_UNITS work units
+ * (units = H * ceil(total Q tiles / 2)); larger ones return
+ * BSATTN_ERR_CAPACITY before any CUDA call (use bsattn_fwd with a workspace).
+ * Setup: the first call on each device resolves the scratch array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  Zeroing: the claim counter in the scratch is
+ * reset on the stream by the scheduling pass of every call.
+ * Concurrency: all calls on one device share the one scratch array, so calls
+ * that may overlap (different streams, or threads without ordering) race on it
+ * and must not be issued.
+ */
+#define BSATTN_STATIC_SCRATCH_UNITS 65536
+bsattn_status bsattn_fwd_static_scratch(const void *q, const void *k, const void *v, int32_t B,
+                                        int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                        const bsattn_meta *meta, const int32_t *kv_valid_len,
+                                        bsattn_mask_kind kind, const bsattn_mask_params *mp,
+                                        float softmax_scale, void *out, bsattn_out_dtype out_dtype,
+                                        float *lse, int32_t *err_flag, void *stream);
 
 /* Human-readable name of a status code (static string). */
 const char *bsattn_status_string(bsattn_status status);

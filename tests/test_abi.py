@@ -44,6 +44,7 @@ def test_abi_version_and_status_strings():
     assert bsa.status_string(bsa.BSATTN_ERR_INVALID_ARG) == "BSATTN_ERR_INVALID_ARG"
     assert bsa.status_string(bsa.BSATTN_ERR_UNSUPPORTED) == "BSATTN_ERR_UNSUPPORTED"
     assert bsa.status_string(bsa.BSATTN_ERR_CUDA) == "BSATTN_ERR_CUDA"
+    assert bsa.status_string(bsa.BSATTN_ERR_CAPACITY) == "BSATTN_ERR_CAPACITY"
     assert bsa.status_string(99) == "BSATTN_ERR_UNKNOWN"
 
 
@@ -132,3 +133,23 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _binding.library()
+
+
+def test_static_scratch_capacity_and_validation():
+    """The fixed-scratch forward rejects problems beyond its capacity (and bad
+    metadata) before any CUDA call."""
+    text = open(HEADER).read()
+    cap = int(re.search(r"#define BSATTN_STATIC_SCRATCH_UNITS (\d+)", text).group(1))
+    assert cap == bsa.BSATTN_STATIC_SCRATCH_UNITS
+
+    def call(meta):
+        return bsa.bsattn_fwd_static_scratch(
+            q=FAKE, k=FAKE, v=FAKE, B=1, seqlen_q=meta.num_m * 128, seqlen_k=256, H=meta.H, D=128,
+            cu_seqlens_q=None, cu_seqlens_k=None, meta=meta, kv_valid_len=None,
+            kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, out=FAKE,
+            out_dtype=bsa.OUT_BF16, lse=FAKE, err_flag=None, stream=0)
+
+    # H * ceil(num_m / 2) units: 2 * 65538 / 2 = cap + 2 > cap
+    assert call(_meta(H=2, num_m=cap + 2)) == bsa.BSATTN_ERR_CAPACITY
+    assert call(_meta(full_idx=None)) == INV
+    assert call(_meta(tile_m=64)) == UNS
