@@ -276,7 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         regs_release<kCtrlRegs>();
         // ------------------------------------------------------- producer --
-        if (lane == 0) {
+        // The whole warp runs the producer's control flow in step (list reads are
+        // broadcast loads); lane 0 alone arms the barriers and issues the copies.
+        const uint32_t lead = lane == 0 ? 1u : 0u;
+        {
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                BSATTN_FLAG_TIMEOUT))
                     goto producer_done;
                 const UnitDesc d = udesc[slot];
-                mbar_arrive(bar(C::bUE + slot));
+                mbar_arrive_lead(lead, bar(C::bUE + slot));
                 const int u = d.u;
                 if (u < 0) break;
                 unit_ring[uc % kUnitRing] = u;
@@ -302,12 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    BSATTN_FLAG_TIMEOUT))
                         goto producer_done;
                     if (ti[t].valid) {
-                        mbar_arrive_expect_tx(bar(C::bQF + t), C::kTileBytes);
+                        mbar_arrive_expect_tx_lead(lead, bar(C::bQF + t), C::kTileBytes);
                         for (int x = 0; x < C::kSub; ++x)
-                            tma_load_3d(sQ + t * C::kTileBytes + x * kSubTileBytes, &tq,
+                            tma_load_3d_lead(lead, sQ + t * C::kTileBytes + x * kSubTileBytes, &tq,
                                         bar(C::bQF + t), x * 64, h, ti[t].qrow0);
                     } else {
-                        mbar_arrive(bar(C::bQF + t));
+                        mbar_arrive_lead(lead, bar(C::bQF + t));
                     }
                     if (t == 0) ++qn0;
                     else ++qn1;
@@ -378,18 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p0) it.lim0 = min(min(kTile, ti[0].sk - c0 * kTile), vl0);
                     if (p1) it.lim1 = min(min(kTile, ti[1].sk - c1 * kTile), vl1);
                     items[ks] = it;
-                    mbar_arrive_expect_tx(bar(C::bKF + ks), C::kTileBytes);
+                    mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
                     for (int x = 0; x < C::kSub; ++x)
-                        tma_load_3d(sK + ks * C::kTileBytes + x * kSubTileBytes, &tk, bar(C::bKF + ks),
+                        tma_load_3d_lead(lead, sK + ks * C::kTileBytes + x * kSubTileBytes, &tk, bar(C::bKF + ks),
                                     x * 64, h, it.krow);
                     ++kc;
                     const uint32_t vs = vc % C::kStagesV;
                     if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
                         goto producer_done;
-                    mbar_arrive_expect_tx(bar(C::bVF + vs), C::kTileBytes);
+                    mbar_arrive_expect_tx_lead(lead, bar(C::bVF + vs), C::kTileBytes);
                     for (int x = 0; x < C::kSub; ++x)
-                        tma_load_3d(sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
+                        tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
                                     x * 64, h, it.krow);
                     ++vc;
                 }
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     end.lim0 = end.lim1 = 0;
                     end.pad0 = end.pad1 = 0;
                     items[ks] = end;
-                    mbar_arrive(bar(C::bKF + ks));
+                    mbar_arrive_lead(lead, bar(C::bKF + ks));
                     ++kc;
                 }
                 ++uc;
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stop.lim0 = stop.lim1 = 0;
                 stop.pad0 = stop.pad1 = 0;
                 items[ks] = stop;
-                mbar_arrive(bar(C::bKF + ks));
+                mbar_arrive_lead(lead, bar(C::bKF + ks));
                 ++kc;
             }
         producer_done:
@@ -441,7 +444,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         regs_release<kCtrlRegs>();
         // ---------------------------------------------------- MMA issuer --
-        if (lane == 0) {
+        // The whole warp runs the issuer's control flow in step (waits, item reads
+        // and bookkeeping are warp-uniform); lane 0 alone issues the MMAs, commits
+        // and arrivals, through predicated instructions.
+        const uint32_t lead = lane == 0 ? 1u : 0u;
+        {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
             // Descriptors are built once; per K step only the 16-byte-unit start
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acc0 = first_pv[t] ? 0u : 1u;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 32; ++kk)
-                    mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
+                    mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                            kk > 0 ? 1u : acc0);
                 if (!mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
                                BSATTN_FLAG_TIMEOUT))
@@ -488,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = kTile / 32; kk < kTile / 16; ++kk)
-                    mma_ts(o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
+                    mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
                 first_pv[t] = false;
-                if (pend[1 - t] != pend[t]) mma_commit(bar(C::bVE + vs));
+                if (pend[1 - t] != pend[t]) mma_commit_lead(lead, bar(C::bVE + vs));
                 pend[t] = -1;
                 return true;
             };
@@ -507,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sinfo[t].n = n;
                 sinfo[t].lim = lim;
                 sinfo[t].flags = fl;
-                mma_commit(bar(C::bSR + t));
-                mbar_arrive(bar(C::bSR + t));
+                mma_commit_lead(lead, bar(C::bSR + t));
+                mbar_arrive_lead(lead, bar(C::bSR + t));
                 return true;
             };
             while (ok) {
@@ -546,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
-                        if (!q_released[t]) mma_commit(bar(C::bQE + t));
-                    mbar_arrive(bar(C::bKE + ks));
+                        if (!q_released[t]) mma_commit_lead(lead, bar(C::bQE + t));
+                    mbar_arrive_lead(lead, bar(C::bKE + ks));
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         if (ok) ok = signal_s(t, -1, 0, kSEnd);
@@ -582,13 +589,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                        mma_ss(s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                        mma_ss_lead(lead, s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     const uint32_t sfl = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
                                          ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
                     if (!(ok = signal_s(t, t ? it.n1 : it.n0, t ? it.lim1 : it.lim0, sfl))) break;
                     if (it.flags & (t ? kLast1 : kLast0)) {
-                        mma_commit(bar(C::bQE + t));  // no further S_t in this unit
+                        mma_commit_lead(lead, bar(C::bQE + t));  // no further S_t in this unit
                         q_released[t] = true;
                     }
                     pend[t] = (int)vc;
@@ -600,12 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 2; ++t)
                     if (ok && !(it.flags & (t ? kPart1 : kPart0)) && pend[t] >= 0) ok = issue_pv(t);
                 if (!ok) break;
-                mma_commit(bar(C::bKE + ks));
+                mma_commit_lead(lead, bar(C::bKE + ks));
                 ++kc;
                 ++vc;
             }
             // Wait until every tcgen05 operation issued above has completed.
-            mma_commit(bar(C::bDrain));
+            mma_commit_lead(lead, bar(C::bDrain));
             mbar_wait_drain(bar(C::bDrain), 0);
         }
     } else if (warp == 3) {
@@ -615,10 +622,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // producer.  Units come either from a fixed stride over the CTAs, or, with a
         // schedule, from an order array claimed slot by slot through an atomic
         // counter.
-        if (lane == 0) {
+        // The whole warp runs in step; lane 0 alone claims (the slot is broadcast)
+        // and arrives.
+        const uint32_t lead = lane == 0 ? 1u : 0u;
+        auto claim_slot = [&]() -> uint32_t {
+            uint32_t pos = 0;
+            if (lead) pos = atomicAdd(p.sched_counter, 1u);
+            return __shfl_sync(0xffffffffu, pos, 0);
+        };
+        {
             int u;
             if (p.dynamic) {
-                const uint32_t pos = atomicAdd(p.sched_counter, 1u);
+                const uint32_t pos = claim_slot();
                 u = pos < (uint32_t)p.num_units ? __ldg(p.sched_order + pos) : -1;
             } else {
                 u = (int)blockIdx.x < p.num_units ? (int)blockIdx.x : -1;
@@ -631,10 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 UnitDesc &d = udesc[slot];
                 d.u = u;
                 if (u < 0) {
-                    mbar_arrive(bar(C::bUF + slot));
+                    mbar_arrive_lead(lead, bar(C::bUF + slot));
                     break;
                 }
-                const uint32_t claim = p.dynamic ? atomicAdd(p.sched_counter, 1u) : 0u;
+                const uint32_t claim = p.dynamic ? claim_slot() : 0u;
                 const int h = u / p.pairs_per_head;
                 const int pr = u - h * p.pairs_per_head;
 #pragma unroll
@@ -662,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     d.e1[2 * t + 1] = f1;
                     d.vl[t] = vl;
                 }
-                mbar_arrive(bar(C::bUF + slot));
+                mbar_arrive_lead(lead, bar(C::bUF + slot));
                 if (p.dynamic)
                     u = claim < (uint32_t)p.num_units ? __ldg(p.sched_order + claim) : -1;
                 else
