@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-meta-formats", action="store_true",
+                    help="skip timing the bitmask / BSR metadata entry points")
     ap.add_argument("--heads", type=int, default=0,
                     help="keep only the first N heads (a smaller case for profiling)")
     return ap.parse_args()
@@ -180,6 +182,61 @@ def cpu_baseline(wl, q, k, v, seconds, threads=None):
             f"drawn at random from the workload: {done_flop / 1e9:.1f} GFLOP of computed tiles "
             f"in {elapsed:.1f} s")
     return value, threads, desc
+
+
+def time_meta_formats(wl, dw, meta, err, stream, iters=20):
+    """The metadata kernel fed by each selection format (byte map, packed bitmask
+    words, BSR rows) on the benchmark workload, outside the timed region: mean ms
+    over `iters` launches and achieved GB/s over the bytes each must move (its
+    input and the two -1-padded lists and counts it writes; the valid lengths,
+    read once per selected mask tile, are left out)."""
+    import numpy as np
+    import torch
+    import block_sparse_flashattention_gb300 as bsa
+    from workloads.formats import to_bitmask, to_bsr
+    words, W = to_bitmask(wl, wl.block_map)
+    indptr, indices = to_bsr(wl, wl.block_map)
+    dev = dw.q.device
+    d_words = torch.from_numpy(words.view(np.int32)).to(dev)
+    d_indptr = torch.from_numpy(indptr).to(dev)
+    d_indices = torch.from_numpy(indices).to(dev)
+    sq, sk = dw.seqlens()
+    rows = words.shape[0]
+    out_bytes = 2 * int(wl.block_map.size) * 4 + 2 * rows * 4   # both lists (num_n per row) + counts
+    in_bytes = {"byte_map": int(wl.block_map.size), "bitmask": int(words.nbytes),
+                "bsr": int(indptr.nbytes + indices.nbytes)}
+    common = dict(cu_seqlens_q=dw.cu_q, cu_seqlens_k=dw.cu_k, seqlen_q=sq, seqlen_k=sk,
+                  kv_valid_len=dw.vl, kind=wl.kind, mask_params=dw.mask_params, meta=meta,
+                  err_flag=err, stream=stream.cuda_stream)
+
+    def call(fmt):
+        if fmt == "byte_map":
+            dw.build_meta(meta, err_flag=err)
+            return
+        if fmt == "bitmask":
+            st = bsa.bsattn_build_meta_bitmask(d_words, W, **common)
+        else:
+            st = bsa.bsattn_build_meta_bsr(d_indptr, d_indices, **common)
+        if st != bsa.BSATTN_OK:
+            raise RuntimeError(f"{fmt}: {bsa.status_string(st)}")
+
+    out = {}
+    for fmt in ("byte_map", "bitmask", "bsr"):
+        for _ in range(3):
+            call(fmt)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            call(fmt)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / iters
+        nbytes = in_bytes[fmt] + out_bytes
+        out[fmt] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())} after the metadata formats")
+    return out
 
 
 def run_reference(args):
@@ -348,6 +405,7 @@ def run_native(args):
     e2e_value = ws * flop_step * K / (e2e_ms * 1e-3) / 1e12
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())}")
+    meta_formats = time_meta_formats(wl, dw, meta, err, stream) if not args.no_meta_formats else None
 
     if rank != 0:
         if pg:
@@ -400,6 +458,7 @@ def run_native(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
+        "meta_formats": meta_formats,
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }

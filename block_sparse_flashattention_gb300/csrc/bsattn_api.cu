@@ -99,47 +99,16 @@ int num_sms_current_device() {
     return cache[dev];
 }
 
-}  // namespace
-
-extern "C" {
-
-const char *bsattn_status_string(bsattn_status s) {
-    switch (s) {
-    case BSATTN_OK: return "BSATTN_OK";
-    case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
-    case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
-    case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
-    case BSATTN_ERR_CAPACITY: return "BSATTN_ERR_CAPACITY";
-    default: return "BSATTN_ERR_UNKNOWN";
-    }
-}
-
-int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
-
-bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
-    if (!bytes) return BSATTN_ERR_INVALID_ARG;
-    *bytes = 0;
-    bsattn_status st = check_meta(meta);
-    if (st != BSATTN_OK) return st;
-    const long long total_m =
-        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
-    const long long units = (long long)meta->H * cdiv(total_m, 2);
-    if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
-    *bytes = (size_t)(kWorkspaceHeader + 4 * units);
-    return BSATTN_OK;
-}
-
-bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
-                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
-                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
-                                const bsattn_mask_params *mp, const bsattn_meta *meta,
-                                int32_t *err_flag, void *stream) {
+// Validation and launch shared by the three metadata entry points; `p` arrives
+// with its selection source set.
+bsattn_status build_meta_impl(bsattn::MetaParams p, const int32_t *cu_seqlens_q,
+                              const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
+                              const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                              const bsattn_mask_params *mp, const bsattn_meta *meta,
+                              int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
-    if (!block_map) return BSATTN_ERR_INVALID_ARG;
-    bsattn::MetaParams p = {};
-    p.map = block_map;
     p.varlen = meta->varlen;
     p.B = meta->B;
     p.H = meta->H;
@@ -182,6 +151,84 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
     p.err = err_flag;
     cudaError_t e = bsattn::launch_meta(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bsattn_status_string(bsattn_status s) {
+    switch (s) {
+    case BSATTN_OK: return "BSATTN_OK";
+    case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
+    case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
+    case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
+    case BSATTN_ERR_CAPACITY: return "BSATTN_ERR_CAPACITY";
+    default: return "BSATTN_ERR_UNKNOWN";
+    }
+}
+
+int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
+
+bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
+    if (!bytes) return BSATTN_ERR_INVALID_ARG;
+    *bytes = 0;
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    const long long total_m =
+        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
+    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
+    *bytes = (size_t)(kWorkspaceHeader + 4 * units);
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
+                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
+                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                int32_t *err_flag, void *stream) {
+    if (!block_map) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcByteMap;
+    p.map = block_map;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_build_meta_bitmask(const uint32_t *words, int32_t words_per_row,
+                                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                        int32_t seqlen_q, int32_t seqlen_k,
+                                        const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                        const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                        int32_t *err_flag, void *stream) {
+    if (!words || words_per_row <= 0) return BSATTN_ERR_INVALID_ARG;
+    // batched rows must hold num_n bits; varlen rows are checked per sequence on the device
+    if (meta && !meta->varlen && (long long)words_per_row * 32 < meta->num_n) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcBitmask;
+    p.words = words;
+    p.words_per_row = words_per_row;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_build_meta_bsr(const int32_t *block_indptr, const int32_t *block_indices,
+                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                    int32_t seqlen_q, int32_t seqlen_k, const int32_t *kv_valid_len,
+                                    bsattn_mask_kind kind, const bsattn_mask_params *mp,
+                                    const bsattn_meta *meta, int32_t *err_flag, void *stream) {
+    if (!block_indptr || !block_indices) return BSATTN_ERR_INVALID_ARG;
+    if (seqlen_k <= 0) return BSATTN_ERR_INVALID_ARG;  // sizes the per-row bit set
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcBsr;
+    p.indptr = block_indptr;
+    p.indices = block_indices;
+    const long long nn_max = cdiv(seqlen_k, kTile);
+    p.bitset_words = (int)((nn_max + 31) / 32);
+    if ((long long)p.bitset_words * 8 * 4 > 200 * 1024) return BSATTN_ERR_UNSUPPORTED;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
 }
 
 bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,

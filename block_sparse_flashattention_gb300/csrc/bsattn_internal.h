@@ -12,8 +12,17 @@ namespace bsattn {
 
 constexpr int kTile = 128;  // tile_m = tile_n = 128 in this build
 
+// Where the metadata kernel reads which KV tiles a Q-tile row selects.
+enum MetaSource { kSrcByteMap = 0, kSrcBitmask = 1, kSrcBsr = 2 };
+
 struct MetaParams {
-    const uint8_t *map;
+    int src;                       // MetaSource
+    const uint8_t *map;            // byte map, laid out like the index lists
+    const uint32_t *words;         // bitmask: [rows][words_per_row], bit n % 32 of word n / 32
+    int words_per_row;
+    const int32_t *indptr;         // BSR: [rows + 1] into indices
+    const int32_t *indices;        // BSR: selected KV tiles of each row, any order
+    int bitset_words;              // BSR: 32-bit words of the per-warp bit set
     int varlen, B, H;
     int num_m, num_n;              // batched sizes (varlen: num_n = kv_valid_len stride)
     int total_m, total_n;          // varlen packed sizes as allocated by the caller

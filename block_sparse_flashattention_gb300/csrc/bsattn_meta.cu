@@ -1,7 +1,10 @@
 // Metadata kernels: varlen offsets and the boolean-block-map -> full / mask list
 // compaction ("[CuTe,Flex] varlen blocksparsity", flash-attention #2224,
 // description and review; list format from "Dense FlashAttention vs Block-Sparse
-// Attention", section 2).
+// Attention", section 2).  The selection may also come as packed 32-bit bitmask
+// words or as BSR indptr / indices rows ("feat(prims-ts): support
+// proxy-compensated block-sparse attention", FlashInfer #4872, bitmask format);
+// all three give the same lists.
 //
 // A selected KV tile is classified over the rectangle of (query row, key) pairs
 // it covers: full if the token predicate holds on every pair, mask if on some,
@@ -126,7 +129,9 @@ __device__ int classify(const MetaParams &p, const RowGeom &g, int n) {
 
 // One warp per (b, h, m) row: lanes take 32 consecutive block ids from the top
 // down, classify them, and compact the ballots into the two descending lists.
+// A BSR row is first turned into a bit set in the warp's shared memory.
 __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p) {
+    extern __shared__ uint32_t bitset_smem[];
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const long long rows =
@@ -177,7 +182,45 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
     }
     if (g.i_max < g.i_min) return;  // cannot happen for m < num_m(b)
 
-    const uint8_t *map = p.map + idx_at;
+    // selection source of this row
+    const uint8_t *map = p.map ? p.map + idx_at : nullptr;
+    const uint32_t *words = nullptr;
+    int nbits = nn;  // tiles the row's selection covers
+    uint32_t *bits = bitset_smem + (threadIdx.x >> 5) * p.bitset_words;
+    if (p.src == kSrcBitmask) {
+        words = p.words + cnt_at * p.words_per_row;
+        if ((long long)p.words_per_row * 32 < nn) {  // the row's words cannot cover its tiles
+            nbits = p.words_per_row * 32;
+            if (lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_COUNT);
+        }
+    } else if (p.src == kSrcBsr) {
+        const int nw = (nn + 31) >> 5;
+        if (nw > p.bitset_words) {  // more tiles than the bit set holds (sizes disagree)
+            nbits = p.bitset_words * 32;
+            if (lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_COUNT);
+        }
+        for (int w = lane; w < p.bitset_words; w += 32) bits[w] = 0u;
+        __syncwarp();
+        const long long a = p.indptr[cnt_at], z = p.indptr[cnt_at + 1];
+        if (z < a) {
+            if (lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_COUNT);
+        } else {
+            bool bad = false;
+            for (long long e = a + lane; e < z; e += 32) {
+                const int32_t n = p.indices[e];
+                if (n >= 0 && n < nbits) atomicOr(&bits[n >> 5], 1u << (n & 31));
+                else bad = true;
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_INDEX);
+        }
+        __syncwarp();
+    }
+    auto selected = [&](int n) -> bool {
+        if (n >= nbits) return false;
+        if (p.src == kSrcBitmask) return (__ldg(words + (n >> 5)) >> (n & 31)) & 1u;
+        if (p.src == kSrcBsr) return (bits[n >> 5] >> (n & 31)) & 1u;
+        return map[n] != 0;
+    };
     int32_t *fidx = p.full_idx + idx_at;
     int32_t *midx = p.mask_idx + idx_at;
     int nf = 0, nmk = 0;
@@ -185,7 +228,7 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
     for (int top = nn - 1; top >= 0; top -= 32) {
         const int n = top - lane;
         int cls = 0;
-        if (n >= 0 && map[n]) cls = classify(p, g, n);
+        if (n >= 0 && selected(n)) cls = classify(p, g, n);
         const unsigned fb = __ballot_sync(0xffffffffu, cls == 2);
         const unsigned mb = __ballot_sync(0xffffffffu, cls == 1);
         if (cls == 2) fidx[nf + __popc(fb & lt)] = n;
@@ -214,7 +257,14 @@ cudaError_t launch_meta(const MetaParams &p, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    bsattn_meta_classify_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
+    const size_t smem = p.src == kSrcBsr ? (size_t)8 * p.bitset_words * sizeof(uint32_t) : 0;
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(bsattn_meta_classify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    bsattn_meta_classify_kernel<<<(unsigned)blocks, 256, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

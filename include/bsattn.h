@@ -134,6 +134,58 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
                                 int32_t *err_flag, void *stream);
 
 /*
+ * bsattn_build_meta_bitmask -- bsattn_build_meta with the selected KV tiles of
+ * each Q-tile row given as packed 32-bit words ("feat(prims-ts): support
+ * proxy-compensated block-sparse attention", FlashInfer #4872, bitmask format:
+ * one bit per semantic KV block; padding bits past the last block are ignored).
+ * The lists written are identical to those bsattn_build_meta writes for the
+ * equivalent byte map.
+ *
+ * words          device uint32 [rows][words_per_row]; KV tile n of a row is
+ *                selected iff bit (n % 32) of word (n / 32) is set (least
+ *                significant bit first).  Rows are ordered like the count arrays:
+ *                batched (b, h, m) -> (b * H + h) * num_m + m; varlen
+ *                (h, packed Q tile T) -> h * total_m_blocks + T.  Bits for
+ *                tiles n >= num_n(b) are ignored.
+ * words_per_row  > 0; batched: at least ceil(num_n / 32) (else
+ *                BSATTN_ERR_INVALID_ARG); varlen: a sequence with more KV tiles
+ *                than 32 * words_per_row sets BSATTN_FLAG_BAD_COUNT and only its
+ *                first 32 * words_per_row tiles can be selected.
+ * Other arguments and errors as for bsattn_build_meta.
+ */
+bsattn_status bsattn_build_meta_bitmask(const uint32_t *words, int32_t words_per_row,
+                                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                        int32_t seqlen_q, int32_t seqlen_k,
+                                        const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                        const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                        int32_t *err_flag, void *stream);
+
+/*
+ * bsattn_build_meta_bsr -- bsattn_build_meta with the selected KV tiles given in
+ * BSR form, block_indptr / block_indices over the Q-tile rows (same page:
+ * canonical BSR block_indptr / block_indices).  The lists written are identical
+ * to those for the equivalent byte map.
+ *
+ * block_indptr   device int32 [rows + 1], rows ordered as for the bitmask form;
+ *                row r selects block_indices[block_indptr[r] .. block_indptr[r+1]).
+ *                A row whose end is below its start selects nothing and sets
+ *                BSATTN_FLAG_BAD_COUNT.
+ * block_indices  device int32 [block_indptr[rows]], KV tile ids of each row in
+ *                any order; a repeated id selects its tile once; an id outside
+ *                [0, num_n(b)) is skipped and sets BSATTN_FLAG_BAD_INDEX.
+ * seqlen_k       must be > 0: batched keys per sequence, varlen total packed keys
+ *                (it bounds num_n(b), which sizes a per-row bit set of
+ *                ceil(ceil(seqlen_k / 128) / 32) words in shared memory;
+ *                BSATTN_ERR_UNSUPPORTED when that exceeds 6400 words).
+ * Other arguments and errors as for bsattn_build_meta.
+ */
+bsattn_status bsattn_build_meta_bsr(const int32_t *block_indptr, const int32_t *block_indices,
+                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                    int32_t seqlen_q, int32_t seqlen_k, const int32_t *kv_valid_len,
+                                    bsattn_mask_kind kind, const bsattn_mask_params *mp,
+                                    const bsattn_meta *meta, int32_t *err_flag, void *stream);
+
+/*
  * bsattn_fwd -- block-sparse attention forward.
  *
  * For each head h, sequence b and query row i (tile m = i / 128), the allowed

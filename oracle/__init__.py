@@ -150,6 +150,68 @@ def build_meta(wl, block_map=None, threads=None) -> dict:
     return out
 
 
+def tile_rows(wl):
+    """Every Q-tile row as (row index, map slice, num_n(b)).  Row indices follow
+    the count arrays: batched (b, h, m) -> (b * H + h) * num_m + m, varlen
+    (h, packed tile T) -> h * total_m_blocks + T; the map slice is where that
+    row's num_n(b) selection bytes sit in the block map."""
+    out = []
+    if not wl.varlen:
+        for b in range(wl.B):
+            for h in range(wl.H):
+                for m in range(wl.num_m):
+                    out.append(((b * wl.H + h) * wl.num_m + m, (b, h, m, slice(0, wl.num_n)), wl.num_n))
+        return out
+    tm = [-(-int(s) // wl.tile_m) for s in wl.seqlens_q]
+    nn = [-(-int(s) // wl.tile_n) for s in wl.seqlens_k]
+    offs = wl.map_row_offsets()
+    cum = np.concatenate([[0], np.cumsum(tm)]).astype(np.int64)
+    for h in range(wl.H):
+        for b in range(wl.B):
+            for m in range(tm[b]):
+                base = int(offs[b]) + m * nn[b]
+                out.append((h * int(cum[-1]) + int(cum[b]) + m, (h, slice(base, base + nn[b])), nn[b]))
+    return out
+
+
+def map_from_bitmask(wl, words, words_per_row):
+    """The block map that packed 32-bit selection words describe ("feat(prims-ts):
+    support proxy-compensated block-sparse attention", FlashInfer #4872, bitmask
+    format): one bit per KV tile of a row, bit n % 32 of word n // 32 (least
+    significant bit first -- a reading: the page does not fix the bit order), and
+    bits past the row's num_n(b) tiles ignored."""
+    words = np.asarray(words, dtype=np.uint32).reshape(-1, words_per_row)
+    bm = np.zeros_like(wl.block_map)
+    for r, sl, nn in tile_rows(wl):
+        n = np.arange(min(nn, 32 * words_per_row))
+        bits = (words[r, n >> 5] >> (n & 31).astype(np.uint32)) & 1
+        row = bm[sl]
+        row[: n.size] = bits.astype(bm.dtype)
+        bm[sl] = row
+    return bm
+
+
+def map_from_bsr(wl, indptr, indices):
+    """The block map that BSR rows describe (same page: canonical block_indptr /
+    block_indices): row r selects the KV tiles indices[indptr[r]:indptr[r+1]], in
+    any order, each once however often it is listed.  Readings: an id outside
+    [0, num_n(b)) selects nothing, and a row whose end lies below its start
+    selects nothing."""
+    indptr = np.asarray(indptr, dtype=np.int64)
+    indices = np.asarray(indices, dtype=np.int64)
+    bm = np.zeros_like(wl.block_map)
+    for r, sl, nn in tile_rows(wl):
+        a, z = int(indptr[r]), int(indptr[r + 1])
+        if z < a:
+            continue
+        ids = indices[a:z]
+        ids = ids[(ids >= 0) & (ids < nn)]
+        row = bm[sl]
+        row[ids] = 1
+        bm[sl] = row
+    return bm
+
+
 def varlen_offsets(wl):
     """(cu_total_m_blocks, cu_block_idx_offsets) for a varlen workload."""
     lib = _load()

@@ -153,3 +153,31 @@ def test_static_scratch_capacity_and_validation():
     assert call(_meta(H=2, num_m=cap + 2)) == bsa.BSATTN_ERR_CAPACITY
     assert call(_meta(full_idx=None)) == INV
     assert call(_meta(tile_m=64)) == UNS
+
+
+def _bmf(fmt, **kw):
+    a = dict(cu_seqlens_q=None, cu_seqlens_k=None, seqlen_q=256, seqlen_k=256, kv_valid_len=None,
+             kind=bsa.MASK_CAUSAL, mask_params=None, meta=_meta(), err_flag=None, stream=0)
+    if fmt == "bitmask":
+        a.update(words=FAKE, words_per_row=1)
+        a.update(kw)
+        return bsa.bsattn_build_meta_bitmask(**a)
+    a.update(block_indptr=FAKE, block_indices=FAKE)
+    a.update(kw)
+    return bsa.bsattn_build_meta_bsr(**a)
+
+
+@pytest.mark.parametrize("fmt,kw,expect", [
+    ("bitmask", dict(words=None), INV),
+    ("bitmask", dict(words_per_row=0), INV),
+    ("bitmask", dict(meta=_meta(num_n=40), seqlen_k=5000), INV),   # 1 word cannot hold 40 tiles
+    ("bitmask", dict(seqlen_k=600), INV),                          # same checks as the byte map
+    ("bitmask", dict(meta=_meta(tile_n=256)), UNS),
+    ("bsr", dict(block_indptr=None), INV),
+    ("bsr", dict(block_indices=None), INV),
+    ("bsr", dict(seqlen_k=0), INV),
+    ("bsr", dict(seqlen_k=600), INV),
+    ("bsr", dict(kind=bsa.MASK_SLIDING_WINDOW), INV),
+])
+def test_format_entry_points_reject_bad_arguments(fmt, kw, expect):
+    assert _bmf(fmt, **kw) == expect
