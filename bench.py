@@ -186,7 +186,8 @@ def cpu_baseline(wl, q, k, v, seconds, threads=None):
 
 def time_meta_formats(wl, dw, meta, err, stream, iters=20):
     """The metadata kernel fed by each selection format (byte map, packed bitmask
-    words, BSR rows) on the benchmark workload, outside the timed region: mean ms
+    words, BSR rows, and, where the workload has one, its native map per 256-token
+    block with per-block valid lengths) on the benchmark workload, outside the timed region: mean ms
     over `iters` launches and achieved GB/s over the bytes each must move (its
     input and the two -1-padded lists and counts it writes; the valid lengths,
     read once per selected mask tile, are left out)."""
@@ -209,9 +210,26 @@ def time_meta_formats(wl, dw, meta, err, stream, iters=20):
                   kv_valid_len=dw.vl, kind=wl.kind, mask_params=dw.mask_params, meta=meta,
                   err_flag=err, stream=stream.cuda_stream)
 
+    native = wl.extra.get("logical_map") if not wl.varlen else None
+    if native is not None:   # the map also exists per 256-token block (2 x 2 tiles)
+        d_blocks = torch.from_numpy(np.ascontiguousarray(native[None] if native.ndim == 3
+                                                         else native)).to(dev)
+        vlb = wl.extra.get("logical_block_valid_len")
+        d_vlb = torch.from_numpy(np.ascontiguousarray(vlb).reshape(wl.B, -1).astype(np.int32)).to(dev) \
+            if vlb is not None else None
+        d_vlt = torch.empty((wl.B, wl.num_n), dtype=torch.int32, device=dev)
+        in_bytes["blocks_2x2"] = int(native.size) + (int(vlb.size) * 4 if vlb is not None else 0)
+
     def call(fmt):
         if fmt == "byte_map":
             dw.build_meta(meta, err_flag=err)
+            return
+        if fmt == "blocks_2x2":
+            st = bsa.bsattn_build_meta_blocks(d_blocks, 2, 2, sq, sk, d_vlb, d_vlt, wl.kind,
+                                              dw.mask_params, meta, err_flag=err,
+                                              stream=stream.cuda_stream)
+            if st != bsa.BSATTN_OK:
+                raise RuntimeError(f"{fmt}: {bsa.status_string(st)}")
             return
         if fmt == "bitmask":
             st = bsa.bsattn_build_meta_bitmask(d_words, W, **common)
@@ -221,7 +239,7 @@ def time_meta_formats(wl, dw, meta, err, stream, iters=20):
             raise RuntimeError(f"{fmt}: {bsa.status_string(st)}")
 
     out = {}
-    for fmt in ("byte_map", "bitmask", "bsr"):
+    for fmt in ("byte_map", "bitmask", "bsr") + (("blocks_2x2",) if native is not None else ()):
         for _ in range(3):
             call(fmt)
         torch.cuda.synchronize(dev)
@@ -232,7 +250,7 @@ def time_meta_formats(wl, dw, meta, err, stream, iters=20):
         b.record(stream)
         torch.cuda.synchronize(dev)
         ms = a.elapsed_time(b) / iters
-        nbytes = in_bytes[fmt] + out_bytes
+        nbytes = in_bytes[fmt] + out_bytes + (wl.B * wl.num_n * 4 if fmt == "blocks_2x2" else 0)
         out[fmt] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())} after the metadata formats")

@@ -61,6 +61,11 @@ def library() -> ctypes.CDLL:
             ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(bsattn_mask_params),
             ctypes.POINTER(bsattn_meta), ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_build_meta.restype = ctypes.c_int
+        lib.bsattn_build_meta_blocks.argtypes = [
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(bsattn_mask_params),
+            ctypes.POINTER(bsattn_meta), ctypes.c_void_p, ctypes.c_void_p]
+        lib.bsattn_build_meta_blocks.restype = ctypes.c_int
         lib.bsattn_build_meta_bitmask.argtypes = [ctypes.c_void_p, ctypes.c_int32] + \
             lib.bsattn_build_meta.argtypes[1:]
         lib.bsattn_build_meta_bitmask.restype = ctypes.c_int
@@ -160,6 +165,20 @@ def bsattn_build_meta(block_map, cu_seqlens_q, cu_seqlens_k, seqlen_q: int, seql
         _ptr(block_map), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(seqlen_q), int(seqlen_k),
         _ptr(kv_valid_len), int(kind), ctypes.byref(mp) if mp is not None else None,
         ctypes.byref(mt), _ptr(err_flag), _stream(stream))
+
+
+def bsattn_build_meta_blocks(block_map, q_block_tiles: int, kv_block_tiles: int, seqlen_q: int,
+                             seqlen_k: int, kv_valid_len_blocks, kv_valid_len_tiles, kind: int,
+                             mask_params: Optional[MaskParams], meta: Meta, err_flag=None,
+                             stream=None) -> int:
+    """Forwards to the C function of the same name; returns its status code."""
+    mp = mask_params.to_c() if mask_params is not None else None
+    mt = meta.to_c()
+    return library().bsattn_build_meta_blocks(
+        _ptr(block_map), int(q_block_tiles), int(kv_block_tiles), int(seqlen_q), int(seqlen_k),
+        _ptr(kv_valid_len_blocks), _ptr(kv_valid_len_tiles), int(kind),
+        ctypes.byref(mp) if mp is not None else None, ctypes.byref(mt), _ptr(err_flag),
+        _stream(stream))
 
 
 def bsattn_build_meta_bitmask(words, words_per_row: int, cu_seqlens_q, cu_seqlens_k,

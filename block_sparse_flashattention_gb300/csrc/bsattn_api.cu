@@ -135,7 +135,7 @@ bsattn_status build_meta_impl(bsattn::MetaParams p, const int32_t *cu_seqlens_q,
     p.cu_tm = meta->cu_total_m_blocks;
     p.cu_off = meta->cu_block_idx_offsets;
     p.vl = kv_valid_len;
-    p.vl_stride = meta->num_n;
+    p.vl_stride = p.vl_per_block ? p.block_n : meta->num_n;
     p.kind = (int)kind;
     if (mp) {
         p.window_left = mp->window_left;
@@ -193,6 +193,33 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
     p.src = bsattn::kSrcByteMap;
     p.map = block_map;
     return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_build_meta_blocks(const uint8_t *block_map, int32_t q_block_tiles,
+                                       int32_t kv_block_tiles, int32_t seqlen_q, int32_t seqlen_k,
+                                       const int32_t *kv_valid_len_blocks,
+                                       int32_t *kv_valid_len_tiles, bsattn_mask_kind kind,
+                                       const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                       int32_t *err_flag, void *stream) {
+    if (!block_map || !meta) return BSATTN_ERR_INVALID_ARG;
+    if (q_block_tiles < 1 || kv_block_tiles < 1 || q_block_tiles > 1024 || kv_block_tiles > 1024)
+        return BSATTN_ERR_INVALID_ARG;
+    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched layouts only
+    if (kv_valid_len_blocks && !kv_valid_len_tiles) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcByteMap;
+    p.map = block_map;
+    p.q_block_tiles = q_block_tiles;
+    p.kv_block_tiles = kv_block_tiles;
+    p.block_m = (int)cdiv(meta->num_m, q_block_tiles);
+    p.block_n = (int)cdiv(meta->num_n, kv_block_tiles);
+    p.kv_block_shift = -1;
+    for (int s = 0; s < 11; ++s)
+        if ((1 << s) == kv_block_tiles) p.kv_block_shift = s;
+    p.vl_tiles_out = kv_valid_len_tiles;
+    p.vl_per_block = kv_valid_len_blocks ? 1 : 0;
+    return build_meta_impl(p, nullptr, nullptr, seqlen_q, seqlen_k, kv_valid_len_blocks, kind, mp,
                            meta, err_flag, stream);
 }
 

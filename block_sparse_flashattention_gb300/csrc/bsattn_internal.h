@@ -23,6 +23,15 @@ struct MetaParams {
     const int32_t *indptr;         // BSR: [rows + 1] into indices
     const int32_t *indices;        // BSR: selected KV tiles of each row, any order
     int bitset_words;              // BSR: 32-bit words of the per-warp bit set
+    // Sparse blocks of q_block_tiles x kv_block_tiles tiles (batched byte map
+    // only; block_n > 0 selects this form): the map is [B, H, block_m, block_n].
+    int q_block_tiles, kv_block_tiles, block_m, block_n;
+    int kv_block_shift;            // log2(kv_block_tiles) when a power of two, else -1
+    // kv_valid_len given per sparse KV block ([B, vl_stride] blocks): tile j of a
+    // block keeps clamp(v - 128 j, 0, 128) keys; vl_tiles_out, if set, receives
+    // the per-tile values [B, num_n].
+    int vl_per_block;
+    int32_t *vl_tiles_out;
     int varlen, B, H;
     int num_m, num_n;              // batched sizes (varlen: num_n = kv_valid_len stride)
     int total_m, total_n;          // varlen packed sizes as allocated by the caller

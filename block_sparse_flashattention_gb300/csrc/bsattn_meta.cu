@@ -71,12 +71,27 @@ struct RowGeom {
     int b;
 };
 
+// Sparse KV block of tile n (a shift for the usual power-of-two block sizes).
+__device__ __forceinline__ int kv_block_of(const MetaParams &p, int n) {
+    return p.kv_block_shift >= 0 ? (n >> p.kv_block_shift) : n / p.kv_block_tiles;
+}
+
+// Valid keys at the start of KV tile n of sequence b: given per tile, or per
+// sparse KV block of kv_block_tiles tiles (tile j of the block keeps
+// clamp(v - 128 j, 0, 128) of the block's v valid keys).
+__device__ __forceinline__ long long tile_valid_len(const MetaParams &p, int b, int n) {
+    if (!p.vl_per_block) return p.vl[(long long)b * p.vl_stride + n];
+    const int blk = kv_block_of(p, n);
+    const long long v = p.vl[(long long)b * p.vl_stride + blk] - (long long)kTile * (n - blk * p.kv_block_tiles);
+    return v < 0 ? 0 : (v > kTile ? kTile : v);
+}
+
 // 0 = drop, 1 = mask list, 2 = full list.
 __device__ int classify(const MetaParams &p, const RowGeom &g, int n) {
     const long long j_lo = (long long)n * kTile, j_end = j_lo + kTile;
     long long j_hi = j_end < g.sk ? j_end : g.sk;
     if (p.vl) {
-        const long long lim = j_lo + (long long)p.vl[(long long)g.b * p.vl_stride + n];
+        const long long lim = j_lo + tile_valid_len(p, g.b, n);
         if (lim < j_hi) j_hi = lim;
     }
     if (j_hi <= j_lo) return 0;
@@ -184,6 +199,14 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
 
     // selection source of this row
     const uint8_t *map = p.map ? p.map + idx_at : nullptr;
+    const bool coarse = p.block_n > 0;  // map given per sparse block
+    if (coarse) {  // batched only: row = (b H + h) num_m + m
+        const long long bh = row / p.num_m;
+        map = p.map + (bh * p.block_m + m / p.q_block_tiles) * p.block_n;
+        if (p.vl_tiles_out && (bh % p.H) == 0 && m == 0)  // once per sequence
+            for (int n = lane; n < nn; n += 32)
+                p.vl_tiles_out[(long long)g.b * nn + n] = p.vl ? (int32_t)tile_valid_len(p, g.b, n) : kTile;
+    }
     const uint32_t *words = nullptr;
     int nbits = nn;  // tiles the row's selection covers
     uint32_t *bits = bitset_smem + (threadIdx.x >> 5) * p.bitset_words;
@@ -219,7 +242,7 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
         if (n >= nbits) return false;
         if (p.src == kSrcBitmask) return (__ldg(words + (n >> 5)) >> (n & 31)) & 1u;
         if (p.src == kSrcBsr) return (bits[n >> 5] >> (n & 31)) & 1u;
-        return map[n] != 0;
+        return (coarse ? map[kv_block_of(p, n)] : map[n]) != 0;
     };
     int32_t *fidx = p.full_idx + idx_at;
     int32_t *midx = p.mask_idx + idx_at;

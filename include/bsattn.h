@@ -134,6 +134,39 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
                                 int32_t *err_flag, void *stream);
 
 /*
+ * bsattn_build_meta_blocks -- bsattn_build_meta for a block map given at a
+ * sparse block size that is a multiple of the 128-token tile ("[CuTe,Flex]
+ * varlen blocksparsity", flash-attention #2224: q_subtile_factor; "[feat] VSA-256
+ * fastpath on Blackwell via FA4 CuTe block-sparse attention", FastVideo #1354:
+ * 256-token blocks run as 128-token tiles).  A sparse block covers q_block_tiles
+ * x kv_block_tiles tiles; tile (m, n) is selected iff its block
+ * (m / q_block_tiles, n / kv_block_tiles) is.  The lists written are identical
+ * to those bsattn_build_meta writes for the expanded per-tile map.
+ *
+ * block_map            device uint8 [B, H, ceil(num_m / q_block_tiles),
+ *                      ceil(num_n / kv_block_tiles)]; nonzero = selected.
+ * q_block_tiles,
+ * kv_block_tiles       tiles per sparse block along Q and KV, 1..1024.
+ * seqlen_q, seqlen_k   per-sequence lengths, as for bsattn_build_meta (batched).
+ * kv_valid_len_blocks  optional device int32 [B, ceil(num_n / kv_block_tiles)]:
+ *                      valid keys at the start of each sparse KV block; tile j
+ *                      of a block keeps clamp(v - 128 j, 0, 128) of them (the
+ *                      VSA split of a 256-token block into min(v, 128) and
+ *                      v - min(v, 128)).
+ * kv_valid_len_tiles   device int32 [B, num_n], written with those per-tile
+ *                      lengths (128 where none are given) for bsattn_fwd; required
+ *                      when kv_valid_len_blocks is given, else optional (NULL).
+ * Varlen metadata -> BSATTN_ERR_UNSUPPORTED.  Other arguments and errors as for
+ * bsattn_build_meta.
+ */
+bsattn_status bsattn_build_meta_blocks(const uint8_t *block_map, int32_t q_block_tiles,
+                                       int32_t kv_block_tiles, int32_t seqlen_q, int32_t seqlen_k,
+                                       const int32_t *kv_valid_len_blocks,
+                                       int32_t *kv_valid_len_tiles, bsattn_mask_kind kind,
+                                       const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                       int32_t *err_flag, void *stream);
+
+/*
  * bsattn_build_meta_bitmask -- bsattn_build_meta with the selected KV tiles of
  * each Q-tile row given as packed 32-bit words ("feat(prims-ts): support
  * proxy-compensated block-sparse attention", FlashInfer #4872, bitmask format:

@@ -174,6 +174,32 @@ def tile_rows(wl):
     return out
 
 
+def expand_blocks(block_map, q_block_tiles, kv_block_tiles, num_m, num_n):
+    """Per-tile map [B, H, num_m, num_n] of a map given per sparse block of
+    q_block_tiles x kv_block_tiles tiles ("[CuTe,Flex] varlen blocksparsity",
+    flash-attention #2224, q_subtile_factor; "[feat] VSA-256 fastpath",
+    FastVideo #1354: each 256-token block runs as 128-token tiles): tile (m, n)
+    takes block (m // q_block_tiles, n // kv_block_tiles)."""
+    bm = np.asarray(block_map)
+    out = np.zeros(bm.shape[:2] + (num_m, num_n), dtype=bm.dtype)
+    for m in range(num_m):
+        for n in range(num_n):
+            out[:, :, m, n] = bm[:, :, m // q_block_tiles, n // kv_block_tiles]
+    return out
+
+
+def split_valid_len(valid_blocks, kv_block_tiles, num_n, tile=128):
+    """Per-tile valid lengths [B, num_n] of lengths given per sparse KV block: tile
+    j of a block keeps clamp(v - tile * j, 0, tile) keys (the VSA split of a
+    256-token block into min(v, 128) and v - min(v, 128), FastVideo #1354)."""
+    vb = np.asarray(valid_blocks, dtype=np.int64)
+    out = np.zeros((vb.shape[0], num_n), np.int32)
+    for n in range(num_n):
+        v = vb[:, n // kv_block_tiles] - tile * (n % kv_block_tiles)
+        out[:, n] = np.clip(v, 0, tile)
+    return out
+
+
 def map_from_bitmask(wl, words, words_per_row):
     """The block map that packed 32-bit selection words describe ("feat(prims-ts):
     support proxy-compensated block-sparse attention", FlashInfer #4872, bitmask

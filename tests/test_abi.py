@@ -181,3 +181,20 @@ def _bmf(fmt, **kw):
 ])
 def test_format_entry_points_reject_bad_arguments(fmt, kw, expect):
     assert _bmf(fmt, **kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(block_map=None), INV),
+    (dict(q_block_tiles=0), INV),
+    (dict(kv_block_tiles=2000), INV),
+    (dict(kv_valid_len_blocks=FAKE, kv_valid_len_tiles=None), INV),   # lengths need an output
+    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), UNS),
+    (dict(seqlen_k=600), INV),
+    (dict(meta=_meta(tile_m=64)), UNS),
+])
+def test_block_map_entry_point_rejects_bad_arguments(kw, expect):
+    a = dict(block_map=FAKE, q_block_tiles=2, kv_block_tiles=2, seqlen_q=256, seqlen_k=256,
+             kv_valid_len_blocks=None, kv_valid_len_tiles=None, kind=bsa.MASK_CAUSAL,
+             mask_params=None, meta=_meta(), err_flag=None, stream=0)
+    a.update(kw)
+    assert bsa.bsattn_build_meta_blocks(**a) == expect

@@ -72,3 +72,31 @@ def test_formats_give_identical_lists():
             got = oracle.build_meta(wl, block_map=bm)
             for key in ("full_cnt", "full_idx", "mask_cnt", "mask_idx"):
                 assert np.array_equal(got[key], ref[key]), (wl.name, key)
+
+
+# ---- sparse blocks larger than the tile -----------------------------------
+
+def test_expand_blocks_worked_example():
+    # 2 x 2 tiles per block; 3 Q tiles (the last block row holds one tile), 4 KV tiles
+    coarse = np.array([[[[1, 0], [0, 1]]]], np.uint8)
+    tiles = oracle.expand_blocks(coarse, 2, 2, 3, 4)
+    assert tiles[0, 0].tolist() == [[1, 1, 0, 0], [1, 1, 0, 0], [0, 0, 1, 1]]
+    # 1 x 3: a block of three KV tiles, ragged at the end (5 tiles)
+    coarse = np.array([[[[0, 1]]]], np.uint8)
+    assert oracle.expand_blocks(coarse, 1, 3, 1, 5)[0, 0].tolist() == [[0, 0, 0, 1, 1]]
+
+
+def test_split_valid_len_worked_example():
+    # the 256-token split: min(v, 128) and v - min(v, 128)
+    got = oracle.split_valid_len(np.array([[200, 100, 256, 0]]), 2, 8)
+    assert got.tolist() == [[128, 72, 100, 0, 128, 128, 0, 0]]
+    # three tiles per block
+    assert oracle.split_valid_len(np.array([[300]]), 3, 3).tolist() == [[128, 128, 44]]
+
+
+def test_vsa_native_blocks_reproduce_the_tile_inputs():
+    wl = make_workload(4)
+    logical = wl.extra["logical_map"][None]             # [1, H, 240, 240]
+    v = wl.extra["logical_block_valid_len"][None]       # [1, 240]
+    assert np.array_equal(oracle.expand_blocks(logical, 2, 2, wl.num_m, wl.num_n), wl.block_map)
+    assert np.array_equal(oracle.split_valid_len(v, 2, wl.num_n), wl.kv_valid_len)
