@@ -49,7 +49,7 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-meta-formats", action="store_true",
-                    help="skip timing the bitmask / BSR metadata entry points")
+                    help="skip the side measurements (metadata formats, proxy A/B)")
     ap.add_argument("--heads", type=int, default=0,
                     help="keep only the first N heads (a smaller case for profiling)")
     return ap.parse_args()
@@ -257,6 +257,72 @@ def time_meta_formats(wl, dw, meta, err, stream, iters=20):
     return out
 
 
+def time_proxy(wl, dw, err, stream, iters=10):
+    """Proxy-compensation A/B on the benchmark map with identical inputs: the exact
+    forward against the proxy forward (summaries of every omitted KV tile), both
+    on metadata built with mask kind none and no valid lengths (the proxy mode
+    needs a dense mask), plus the time of the KV summaries kernel."""
+    import math
+    import numpy as np
+    import torch
+    import block_sparse_flashattention_gb300 as bsa
+    from workloads.formats import to_bitmask
+    if wl.varlen or wl.kind != bsa.MASK_NONE:
+        return None
+    dev = dw.q.device
+    sq, sk = dw.seqlens()
+    meta = dw.alloc_meta()
+    st = bsa.bsattn_build_meta(dw.block_map, None, None, sq, sk, None, bsa.MASK_NONE, None, meta,
+                               err, stream.cuda_stream)
+    if st != bsa.BSATTN_OK:
+        raise RuntimeError(bsa.status_string(st))
+    nn = math.ceil(sk / 128)
+    ks = torch.empty((wl.B, nn, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    words, W = to_bitmask(wl, wl.block_map)
+    d_words = torch.from_numpy(words.view(np.int32)).to(dev)
+    out = torch.empty(dw.q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.B, wl.H, sq), dtype=torch.float32, device=dev)
+    ws = bsa.alloc_workspace(meta, dev)
+
+    def summaries():
+        st = bsa.bsattn_kv_summaries(dw.k, dw.v, wl.B, sk, wl.H, wl.D, ks, vs, stream.cuda_stream)
+        if st != bsa.BSATTN_OK:
+            raise RuntimeError(bsa.status_string(st))
+
+    def exact():
+        st = bsa.bsattn_fwd(dw.q, dw.k, dw.v, wl.B, sq, sk, wl.H, wl.D, None, None, meta, None,
+                            bsa.MASK_NONE, None, wl.scale, out, bsa.OUT_BF16, lse, workspace=ws,
+                            err_flag=err, stream=stream.cuda_stream)
+        if st != bsa.BSATTN_OK:
+            raise RuntimeError(bsa.status_string(st))
+
+    def proxy():
+        st = bsa.bsattn_fwd_proxy(dw.q, dw.k, dw.v, wl.B, sq, sk, wl.H, wl.D, meta, d_words, W, ks,
+                                  vs, wl.scale, out, bsa.OUT_BF16, lse, workspace=ws, err_flag=err,
+                                  stream=stream.cuda_stream)
+        if st != bsa.BSATTN_OK:
+            raise RuntimeError(bsa.status_string(st))
+
+    res = {}
+    for name, fn in (("summaries", summaries), ("exact", exact), ("proxy", proxy)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name + "_ms"] = a.elapsed_time(b) / iters
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())} in the proxy A/B")
+    res["overhead"] = res["proxy_ms"] / res["exact_ms"] - 1.0
+    res["note"] = "benchmark map, mask kind none, no valid lengths; summaries outside both arms"
+    return res
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -424,6 +490,7 @@ def run_native(args):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())}")
     meta_formats = time_meta_formats(wl, dw, meta, err, stream) if not args.no_meta_formats else None
+    proxy_ab = time_proxy(wl, dw, err, stream) if not args.no_meta_formats else None
 
     if rank != 0:
         if pg:
@@ -477,6 +544,7 @@ def run_native(args):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
         "meta_formats": meta_formats,
+        "proxy_ab": proxy_ab,
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }

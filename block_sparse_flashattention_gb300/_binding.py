@@ -61,6 +61,10 @@ def library() -> ctypes.CDLL:
             ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(bsattn_mask_params),
             ctypes.POINTER(bsattn_meta), ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_build_meta.restype = ctypes.c_int
+        lib.bsattn_kv_summaries.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.bsattn_kv_summaries.restype = ctypes.c_int
         lib.bsattn_build_meta_blocks.argtypes = [
             ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(bsattn_mask_params),
@@ -79,6 +83,13 @@ def library() -> ctypes.CDLL:
             ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_fwd.restype = ctypes.c_int
+        lib.bsattn_fwd_proxy.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(bsattn_meta),
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+            ctypes.c_void_p, ctypes.c_void_p]
+        lib.bsattn_fwd_proxy.restype = ctypes.c_int
         lib.bsattn_fwd_static_scratch.argtypes = lib.bsattn_fwd.argtypes[:18] + [
             ctypes.c_void_p, ctypes.c_void_p]
         lib.bsattn_fwd_static_scratch.restype = ctypes.c_int
@@ -167,6 +178,13 @@ def bsattn_build_meta(block_map, cu_seqlens_q, cu_seqlens_k, seqlen_q: int, seql
         ctypes.byref(mt), _ptr(err_flag), _stream(stream))
 
 
+def bsattn_kv_summaries(k, v, B: int, seqlen_k: int, H: int, D: int, k_sum, v_sum,
+                        stream=None) -> int:
+    """Forwards to the C function of the same name; returns its status code."""
+    return library().bsattn_kv_summaries(_ptr(k), _ptr(v), int(B), int(seqlen_k), int(H), int(D),
+                                         _ptr(k_sum), _ptr(v_sum), _stream(stream))
+
+
 def bsattn_build_meta_blocks(block_map, q_block_tiles: int, kv_block_tiles: int, seqlen_q: int,
                              seqlen_k: int, kv_valid_len_blocks, kv_valid_len_tiles, kind: int,
                              mask_params: Optional[MaskParams], meta: Meta, err_flag=None,
@@ -223,6 +241,21 @@ def bsattn_fwd(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int, cu
         ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(out),
         int(out_dtype), _ptr(lse), _ptr(workspace), int(workspace_bytes), _ptr(err_flag),
         _stream(stream))
+
+
+def bsattn_fwd_proxy(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int, meta: Meta,
+                     sel_words, words_per_row: int, k_sum, v_sum, softmax_scale: float, out,
+                     out_dtype: int, lse, workspace=None, workspace_bytes: int = 0, err_flag=None,
+                     stream=None) -> int:
+    """Forwards to the C function of the same name; returns its status code."""
+    mt = meta.to_c()
+    if workspace is not None and not isinstance(workspace, int) and workspace_bytes == 0:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return library().bsattn_fwd_proxy(
+        _ptr(q), _ptr(k), _ptr(v), int(B), int(seqlen_q), int(seqlen_k), int(H), int(D),
+        ctypes.byref(mt), _ptr(sel_words), int(words_per_row), _ptr(k_sum), _ptr(v_sum),
+        float(softmax_scale), _ptr(out), int(out_dtype), _ptr(lse), _ptr(workspace),
+        int(workspace_bytes), _ptr(err_flag), _stream(stream))
 
 
 def bsattn_fwd_static_scratch(q, k, v, B: int, seqlen_q: int, seqlen_k: int, H: int, D: int,

@@ -153,118 +153,20 @@ bsattn_status build_meta_impl(bsattn::MetaParams p, const int32_t *cu_seqlens_q,
     return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
 }
 
-}  // namespace
+struct ProxyArgs {
+    const uint32_t *sel_words;
+    int32_t words_per_row;
+    const void *k_sum, *v_sum;
+};
 
-extern "C" {
-
-const char *bsattn_status_string(bsattn_status s) {
-    switch (s) {
-    case BSATTN_OK: return "BSATTN_OK";
-    case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
-    case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
-    case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
-    case BSATTN_ERR_CAPACITY: return "BSATTN_ERR_CAPACITY";
-    default: return "BSATTN_ERR_UNKNOWN";
-    }
-}
-
-int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
-
-bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
-    if (!bytes) return BSATTN_ERR_INVALID_ARG;
-    *bytes = 0;
-    bsattn_status st = check_meta(meta);
-    if (st != BSATTN_OK) return st;
-    const long long total_m =
-        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
-    const long long units = (long long)meta->H * cdiv(total_m, 2);
-    if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
-    *bytes = (size_t)(kWorkspaceHeader + 4 * units);
-    return BSATTN_OK;
-}
-
-bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
-                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
-                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
-                                const bsattn_mask_params *mp, const bsattn_meta *meta,
-                                int32_t *err_flag, void *stream) {
-    if (!block_map) return BSATTN_ERR_INVALID_ARG;
-    bsattn::MetaParams p = {};
-    p.src = bsattn::kSrcByteMap;
-    p.map = block_map;
-    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
-                           meta, err_flag, stream);
-}
-
-bsattn_status bsattn_build_meta_blocks(const uint8_t *block_map, int32_t q_block_tiles,
-                                       int32_t kv_block_tiles, int32_t seqlen_q, int32_t seqlen_k,
-                                       const int32_t *kv_valid_len_blocks,
-                                       int32_t *kv_valid_len_tiles, bsattn_mask_kind kind,
-                                       const bsattn_mask_params *mp, const bsattn_meta *meta,
-                                       int32_t *err_flag, void *stream) {
-    if (!block_map || !meta) return BSATTN_ERR_INVALID_ARG;
-    if (q_block_tiles < 1 || kv_block_tiles < 1 || q_block_tiles > 1024 || kv_block_tiles > 1024)
-        return BSATTN_ERR_INVALID_ARG;
-    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched layouts only
-    if (kv_valid_len_blocks && !kv_valid_len_tiles) return BSATTN_ERR_INVALID_ARG;
-    bsattn::MetaParams p = {};
-    p.src = bsattn::kSrcByteMap;
-    p.map = block_map;
-    p.q_block_tiles = q_block_tiles;
-    p.kv_block_tiles = kv_block_tiles;
-    p.block_m = (int)cdiv(meta->num_m, q_block_tiles);
-    p.block_n = (int)cdiv(meta->num_n, kv_block_tiles);
-    p.kv_block_shift = -1;
-    for (int s = 0; s < 11; ++s)
-        if ((1 << s) == kv_block_tiles) p.kv_block_shift = s;
-    p.vl_tiles_out = kv_valid_len_tiles;
-    p.vl_per_block = kv_valid_len_blocks ? 1 : 0;
-    return build_meta_impl(p, nullptr, nullptr, seqlen_q, seqlen_k, kv_valid_len_blocks, kind, mp,
-                           meta, err_flag, stream);
-}
-
-bsattn_status bsattn_build_meta_bitmask(const uint32_t *words, int32_t words_per_row,
-                                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                                        int32_t seqlen_q, int32_t seqlen_k,
-                                        const int32_t *kv_valid_len, bsattn_mask_kind kind,
-                                        const bsattn_mask_params *mp, const bsattn_meta *meta,
-                                        int32_t *err_flag, void *stream) {
-    if (!words || words_per_row <= 0) return BSATTN_ERR_INVALID_ARG;
-    // batched rows must hold num_n bits; varlen rows are checked per sequence on the device
-    if (meta && !meta->varlen && (long long)words_per_row * 32 < meta->num_n) return BSATTN_ERR_INVALID_ARG;
-    bsattn::MetaParams p = {};
-    p.src = bsattn::kSrcBitmask;
-    p.words = words;
-    p.words_per_row = words_per_row;
-    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
-                           meta, err_flag, stream);
-}
-
-bsattn_status bsattn_build_meta_bsr(const int32_t *block_indptr, const int32_t *block_indices,
-                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                                    int32_t seqlen_q, int32_t seqlen_k, const int32_t *kv_valid_len,
-                                    bsattn_mask_kind kind, const bsattn_mask_params *mp,
-                                    const bsattn_meta *meta, int32_t *err_flag, void *stream) {
-    if (!block_indptr || !block_indices) return BSATTN_ERR_INVALID_ARG;
-    if (seqlen_k <= 0) return BSATTN_ERR_INVALID_ARG;  // sizes the per-row bit set
-    bsattn::MetaParams p = {};
-    p.src = bsattn::kSrcBsr;
-    p.indptr = block_indptr;
-    p.indices = block_indices;
-    const long long nn_max = cdiv(seqlen_k, kTile);
-    p.bitset_words = (int)((nn_max + 31) / 32);
-    if ((long long)p.bitset_words * 8 * 4 > 200 * 1024) return BSATTN_ERR_UNSUPPORTED;
-    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
-                           meta, err_flag, stream);
-}
-
-bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,
+bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,
                          int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
                          const int32_t *cu_seqlens_k, const bsattn_meta *meta,
                          const int32_t *kv_valid_len, bsattn_mask_kind kind,
                          const bsattn_mask_params *mp, float softmax_scale, void *out,
                          bsattn_out_dtype out_dtype, float *lse, void *workspace,
-                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
+                         size_t workspace_bytes, int32_t *err_flag, void *stream,
+                      const ProxyArgs *proxy) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
@@ -347,10 +249,170 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
     if (!encode_bshd(&tq, q, rows_q, H, D) || !encode_bshd(&tk, k, rows_k > 0 ? rows_k : 1, H, D) ||
         !encode_bshd(&tv, v, rows_k > 0 ? rows_k : 1, H, D))
         return BSATTN_ERR_CUDA;
+    CUtensorMap tks = tk, tvs = tv;  // summary maps: unused unless proxy summaries are given
+    if (proxy) {
+        const long long sum_rows = (long long)B * meta->num_n;
+        if (!encode_bshd(&tks, proxy->k_sum, sum_rows, H, D) ||
+            !encode_bshd(&tvs, proxy->v_sum, sum_rows, H, D))
+            return BSATTN_ERR_CUDA;
+        p.proxy = 1;
+        p.sel_words = proxy->sel_words;
+        p.sel_words_per_row = proxy->words_per_row;
+        p.proxy_tail = seqlen_k - (meta->num_n - 1) * kTile;
+    }
     const int sms = num_sms_current_device();
     if (sms <= 0) return BSATTN_ERR_CUDA;
-    cudaError_t e = bsattn::launch_fwd(p, tq, tk, tv, D, sms, static_cast<cudaStream_t>(stream));
+    cudaError_t e = bsattn::launch_fwd(p, tq, tk, tv, tks, tvs, D, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bsattn_status_string(bsattn_status s) {
+    switch (s) {
+    case BSATTN_OK: return "BSATTN_OK";
+    case BSATTN_ERR_INVALID_ARG: return "BSATTN_ERR_INVALID_ARG";
+    case BSATTN_ERR_UNSUPPORTED: return "BSATTN_ERR_UNSUPPORTED";
+    case BSATTN_ERR_CUDA: return "BSATTN_ERR_CUDA";
+    case BSATTN_ERR_CAPACITY: return "BSATTN_ERR_CAPACITY";
+    default: return "BSATTN_ERR_UNKNOWN";
+    }
+}
+
+int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
+
+bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
+    if (!bytes) return BSATTN_ERR_INVALID_ARG;
+    *bytes = 0;
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    const long long total_m =
+        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
+    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
+    *bytes = (size_t)(kWorkspaceHeader + 4 * units);
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seqlens_q,
+                                const int32_t *cu_seqlens_k, int32_t seqlen_q, int32_t seqlen_k,
+                                const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                int32_t *err_flag, void *stream) {
+    if (!block_map) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcByteMap;
+    p.map = block_map;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_kv_summaries(const void *k, const void *v, int32_t B, int32_t seqlen_k,
+                                  int32_t H, int32_t D, void *k_sum, void *v_sum, void *stream) {
+    if (!k || !v || !k_sum || !v_sum) return BSATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || seqlen_k <= 0 || D <= 0 || (D & 1) || D > 256) return BSATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(k_sum) | reinterpret_cast<uintptr_t>(v_sum)) & 3u)
+        return BSATTN_ERR_INVALID_ARG;
+    if ((long long)B * seqlen_k * H * D > (1LL << 40)) return BSATTN_ERR_INVALID_ARG;
+    const cudaError_t e = bsattn::launch_kv_summary(k, v, B, seqlen_k, H, D, k_sum, v_sum,
+                                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+bsattn_status bsattn_build_meta_blocks(const uint8_t *block_map, int32_t q_block_tiles,
+                                       int32_t kv_block_tiles, int32_t seqlen_q, int32_t seqlen_k,
+                                       const int32_t *kv_valid_len_blocks,
+                                       int32_t *kv_valid_len_tiles, bsattn_mask_kind kind,
+                                       const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                       int32_t *err_flag, void *stream) {
+    if (!block_map || !meta) return BSATTN_ERR_INVALID_ARG;
+    if (q_block_tiles < 1 || kv_block_tiles < 1 || q_block_tiles > 1024 || kv_block_tiles > 1024)
+        return BSATTN_ERR_INVALID_ARG;
+    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched layouts only
+    if (kv_valid_len_blocks && !kv_valid_len_tiles) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcByteMap;
+    p.map = block_map;
+    p.q_block_tiles = q_block_tiles;
+    p.kv_block_tiles = kv_block_tiles;
+    p.block_m = (int)cdiv(meta->num_m, q_block_tiles);
+    p.block_n = (int)cdiv(meta->num_n, kv_block_tiles);
+    p.kv_block_shift = -1;
+    for (int s = 0; s < 11; ++s)
+        if ((1 << s) == kv_block_tiles) p.kv_block_shift = s;
+    p.vl_tiles_out = kv_valid_len_tiles;
+    p.vl_per_block = kv_valid_len_blocks ? 1 : 0;
+    return build_meta_impl(p, nullptr, nullptr, seqlen_q, seqlen_k, kv_valid_len_blocks, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_build_meta_bitmask(const uint32_t *words, int32_t words_per_row,
+                                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                        int32_t seqlen_q, int32_t seqlen_k,
+                                        const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                                        const bsattn_mask_params *mp, const bsattn_meta *meta,
+                                        int32_t *err_flag, void *stream) {
+    if (!words || words_per_row <= 0) return BSATTN_ERR_INVALID_ARG;
+    // batched rows must hold num_n bits; varlen rows are checked per sequence on the device
+    if (meta && !meta->varlen && (long long)words_per_row * 32 < meta->num_n) return BSATTN_ERR_INVALID_ARG;
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcBitmask;
+    p.words = words;
+    p.words_per_row = words_per_row;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_build_meta_bsr(const int32_t *block_indptr, const int32_t *block_indices,
+                                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                    int32_t seqlen_q, int32_t seqlen_k, const int32_t *kv_valid_len,
+                                    bsattn_mask_kind kind, const bsattn_mask_params *mp,
+                                    const bsattn_meta *meta, int32_t *err_flag, void *stream) {
+    if (!block_indptr || !block_indices) return BSATTN_ERR_INVALID_ARG;
+    if (seqlen_k <= 0) return BSATTN_ERR_INVALID_ARG;  // sizes the per-row bit set
+    bsattn::MetaParams p = {};
+    p.src = bsattn::kSrcBsr;
+    p.indptr = block_indptr;
+    p.indices = block_indices;
+    const long long nn_max = cdiv(seqlen_k, kTile);
+    p.bitset_words = (int)((nn_max + 31) / 32);
+    if ((long long)p.bitset_words * 8 * 4 > 200 * 1024) return BSATTN_ERR_UNSUPPORTED;
+    return build_meta_impl(p, cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, kv_valid_len, kind, mp,
+                           meta, err_flag, stream);
+}
+
+bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B, int32_t seqlen_q,
+                         int32_t seqlen_k, int32_t H, int32_t D, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, const bsattn_meta *meta,
+                         const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                         const bsattn_mask_params *mp, float softmax_scale, void *out,
+                         bsattn_out_dtype out_dtype, float *lse, void *workspace,
+                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    return fwd_impl(q, k, v, B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta, kv_valid_len,
+                    kind, mp, softmax_scale, out, out_dtype, lse, workspace, workspace_bytes, err_flag,
+                    stream, nullptr);
+}
+
+bsattn_status bsattn_fwd_proxy(const void *q, const void *k, const void *v, int32_t B,
+                               int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                               const bsattn_meta *meta, const uint32_t *sel_words,
+                               int32_t words_per_row, const void *k_sum, const void *v_sum,
+                               float softmax_scale, void *out, bsattn_out_dtype out_dtype, float *lse,
+                               void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                               void *stream) {
+    if (!meta) return BSATTN_ERR_INVALID_ARG;
+    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched only
+    if (!sel_words || !k_sum || !v_sum) return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_sum) || !aligned16(v_sum)) return BSATTN_ERR_INVALID_ARG;
+    if (words_per_row <= 0 || (long long)words_per_row * 32 < meta->num_n) return BSATTN_ERR_INVALID_ARG;
+    if ((long long)B * meta->num_n > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+    ProxyArgs pa{sel_words, words_per_row, k_sum, v_sum};
+    return fwd_impl(q, k, v, B, seqlen_q, seqlen_k, H, D, nullptr, nullptr, meta, nullptr,
+                    BSATTN_MASK_NONE, nullptr, softmax_scale, out, out_dtype, lse, workspace,
+                    workspace_bytes, err_flag, stream, &pa);
 }
 
 }  // extern "C"

@@ -47,9 +47,10 @@ constexpr uint32_t kSubTileBytes = kTile * 64 * 2;  // 128 rows x 64 bf16 (one 1
 // Item flags (producer -> MMA issuer).
 constexpr uint32_t kPart0 = 1u, kPart1 = 2u, kMask0 = 4u, kMask1 = 8u, kEnd = 16u, kBound0 = 32u,
                    kBound1 = 64u, kLast0 = 128u, kLast1 = 256u,  // kLast_t: tile t's last item
-                   kStop = 512u;                                  // no further units
+                   kStop = 512u,                                  // no further units
+                   kSummary = 1024u;                              // K/V from the tile summaries
 // Per-tile flags (MMA issuer -> softmax).
-constexpr uint32_t kSMask = 1u, kSBound = 2u, kSEnd = 4u, kSStop = 8u;
+constexpr uint32_t kSMask = 1u, kSBound = 2u, kSEnd = 4u, kSStop = 8u, kSSummary = 16u;
 constexpr int kUnitRing = 4;  // unit ids in flight between the producer and the softmax
 
 struct Item {
@@ -216,11 +217,14 @@ __device__ __forceinline__ void cur_init(Cursor &c, const int32_t *ptr, int cnt,
     cur_advance(c, nn, err);
 }
 
-template <int D>
+// kProxy: proxy-compensation build (summary items after each unit); the exact
+// build carries none of that code.
+template <int D, bool kProxy>
 __global__ void __launch_bounds__(kThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tq,
-                      const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv) {
+                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                      const __grid_constant__ CUtensorMap tks,
+                      const __grid_constant__ CUtensorMap tvs) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -372,8 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // A tile whose lists are now exhausted is done with its Q tile after
                     // this item's S: the MMA warp releases that Q buffer early.
-                    if (p0 && max(cm[0].head, cf[0].head) < 0) it.flags |= kLast0;
-                    if (p1 && max(cm[1].head, cf[1].head) < 0) it.flags |= kLast1;
+                    // (with proxy compensation the tile's last item is a summary item)
+                    if (!kProxy && p0 && max(cm[0].head, cf[0].head) < 0) it.flags |= kLast0;
+                    if (!kProxy && p1 && max(cm[1].head, cf[1].head) < 0) it.flags |= kLast1;
                     const uint32_t ks = kc % C::kStagesK;
                     if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
@@ -395,6 +400,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
                                     x * 64, h, it.krow);
                     ++vc;
+                }
+                if constexpr (kProxy) {
+                    // Summary items: every chunk of 128 KV-tile summaries of each tile's
+                    // sequence (row b * num_n + 128 c of the summary tensors), from the
+                    // last chunk down; two tiles of one sequence share each chunk.
+                    const int nc = (p.num_n + kTile - 1) / kTile;
+                    int sc0 = ti[0].valid ? nc - 1 : -1, sc1 = ti[1].valid ? nc - 1 : -1;
+                    while (sc0 >= 0 || sc1 >= 0) {
+                        const long long g0 = sc0 >= 0 ? (long long)ti[0].b * p.num_n + (long long)sc0 * kTile : -1;
+                        const long long g1 = sc1 >= 0 ? (long long)ti[1].b * p.num_n + (long long)sc1 * kTile : -1;
+                        const bool p0 = sc0 >= 0 && g0 >= g1, p1 = sc1 >= 0 && g1 >= g0;
+                        Item it;
+                        it.krow = (int32_t)(p0 ? g0 : g1);
+                        it.n0 = p0 ? sc0 : -1;
+                        it.n1 = p1 ? sc1 : -1;
+                        it.flags = kSummary | (p0 ? kPart0 : 0u) | (p1 ? kPart1 : 0u);
+                        it.lim0 = p0 ? min(kTile, p.num_n - sc0 * kTile) : kTile;
+                        it.lim1 = p1 ? min(kTile, p.num_n - sc1 * kTile) : kTile;
+                        it.pad0 = it.pad1 = 0;
+                        if (p0 && --sc0 < 0) it.flags |= kLast0;
+                        if (p1 && --sc1 < 0) it.flags |= kLast1;
+                        const uint32_t ks = kc % C::kStagesK;
+                        if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                       BSATTN_FLAG_TIMEOUT))
+                            goto producer_done;
+                        items[ks] = it;
+                        mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
+                        for (int x = 0; x < C::kSub; ++x)
+                            tma_load_3d_lead(lead, sK + ks * C::kTileBytes + x * kSubTileBytes, &tks,
+                                             bar(C::bKF + ks), x * 64, h, it.krow);
+                        ++kc;
+                        const uint32_t vs = vc % C::kStagesV;
+                        if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
+                                       BSATTN_FLAG_TIMEOUT))
+                            goto producer_done;
+                        mbar_arrive_expect_tx_lead(lead, bar(C::bVF + vs), C::kTileBytes);
+                        for (int x = 0; x < C::kSub; ++x)
+                            tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tvs,
+                                             bar(C::bVF + vs), x * 64, h, it.krow);
+                        ++vc;
+                    }
                 }
                 {
                     const uint32_t ks = kc % C::kStagesK;
@@ -592,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss_lead(lead, s_tmem, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     const uint32_t sfl = ((it.flags & (t ? kMask1 : kMask0)) ? kSMask : 0u) |
-                                         ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u);
+                                         ((it.flags & (t ? kBound1 : kBound0)) ? kSBound : 0u) |
+                                         ((it.flags & kSummary) ? kSSummary : 0u);
                     if (!(ok = signal_s(t, t ? it.n1 : it.n0, t ? it.lim1 : it.lim0, sfl))) break;
                     if (it.flags & (t ? kLast1 : kLast0)) {
                         mma_commit_lead(lead, bar(C::bQE + t));  // no further S_t in this unit
@@ -731,12 +778,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 float s[128];
+                // Summary items: the sequence's last KV tile, if partial, counts with
+                // its true number of keys; its score column is read on its own (P
+                // overwrites the first half of the S columns).
+                const bool summary = kProxy && (si.flags & kSSummary) != 0;
+                int c_tail = -1;
+                if (summary && p.proxy_tail < kTile) {
+                    const int ct = (p.num_n - 1) - si.n * kTile;
+                    if (ct >= 0 && ct < kTile) c_tail = ct;
+                }
+                uint32_t s_tail_bits = 0u;
                 {
                     uint32_t v0[32], v1[32], v2[32], v3[32];
                     tmem_ld32(lane_addr + s_col + 0, v0);
                     tmem_ld32(lane_addr + s_col + 32, v1);
                     tmem_ld32(lane_addr + s_col + 64, v2);
                     tmem_ld32(lane_addr + s_col + 96, v3);
+                    if (c_tail >= 0) tmem_ld1(lane_addr + s_col + (uint32_t)c_tail, s_tail_bits);
                     tmem_wait_ld();
                     reg_fence(v0);
                     reg_fence(v1);
@@ -750,13 +808,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         s[96 + x] = __uint_as_float(v3[x]);
                     }
                 }
-                if (si.flags & (kSMask | kSBound)) {
+                bool tail_kept = false;
+                if (si.flags & (kSMask | kSBound | (kProxy ? kSSummary : 0u))) {
                     // Keep-mask of the 128 columns as four 32-bit words; columns at or
                     // past si.lim (sequence end, valid length) are always dropped.
                     const int j0 = si.n * kTile;
                     const int lim = si.lim;
                     uint32_t keep[4];
-                    if (!(si.flags & kSMask) || p.kind == BSATTN_MASK_NONE) {
+                    if (summary) {
+                        // keep the summary columns whose tile is not computed exactly
+                        const uint32_t *sw = p.sel_words + ti.cnt_at * p.sel_words_per_row;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int wi = 4 * si.n + w;
+                            const uint32_t sel = wi < p.sel_words_per_row ? __ldg(sw + wi) : 0u;
+                            keep[w] = ~sel & span_bits(0, lim - 32 * w);
+                        }
+                        if (c_tail >= 0) {
+                            const uint32_t kw = (c_tail >> 5) == 0 ? keep[0]
+                                              : (c_tail >> 5) == 1 ? keep[1]
+                                              : (c_tail >> 5) == 2 ? keep[2] : keep[3];
+                            tail_kept = (kw >> (c_tail & 31)) & 1u;
+                        }
+                    } else if (!(si.flags & kSMask) || p.kind == BSATTN_MASK_NONE) {
 #pragma unroll
                         for (int w = 0; w < 4; ++w) keep[w] = span_bits(0, lim - 32 * w);
                     } else if (p.kind == BSATTN_MASK_DOCUMENT) {
@@ -859,7 +933,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p_half(1);
                 publish(1);
                 const float l0 = la0 + lb0, l1 = la1 + lb1;
-                l_run = l_run * alpha + (l0 + l1);
+                float l_item = l0 + l1;
+                if (summary) {
+                    // a summary column stands for the 128 keys of its tile (the tail
+                    // tile for proxy_tail keys)
+                    l_item *= (float)kTile;
+                    if (tail_kept) {
+                        const float pt = ex2_approx(fmaf(__uint_as_float(s_tail_bits), sl2, nm));
+                        l_item += (float)(p.proxy_tail - kTile) * pt;
+                    }
+                }
+                l_run = l_run * alpha + l_item;
                 ++j;
                 if (!(ok = wait_s())) break;
             }
@@ -1035,9 +1119,8 @@ __global__ void __launch_bounds__(1024, 1) bsattn_schedule_kernel(const __grid_c
     }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                         const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
+template <int D, bool kProxy>
+cudaError_t prepare_fwd_kernel() {
     using C = Cfg<D>;
     static int attr_set_for_device[64] = {0};
     int dev = 0;
@@ -1048,14 +1131,24 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
         // The register split inside the kernel assumes exactly kLaunchRegs per
         // thread at launch; refuse to run a build where that does not hold.
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D>);
+        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D, kProxy>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, kProxy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                         const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs,
+                         int num_sms, cudaStream_t stream) {
+    using C = Cfg<D>;
+    cudaError_t e = p.proxy ? prepare_fwd_kernel<D, true>() : prepare_fwd_kernel<D, false>();
+    if (e != cudaSuccess) return e;
     if (p.num_units <= 0) return cudaSuccess;
     if (p.dynamic) {
         const size_t key_bytes = (size_t)p.num_units * sizeof(uint16_t);
@@ -1069,16 +1162,20 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
         if (e != cudaSuccess) return e;
     }
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-    bsattn_fwd_kernel<D><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv);
+    if (p.proxy)
+        bsattn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
+    else
+        bsattn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                       const CUtensorMap &tv, int D, int num_sms, cudaStream_t stream) {
-    if (D == 128) return launch_fwd_d<128>(p, tq, tk, tv, num_sms, stream);
-    if (D == 64) return launch_fwd_d<64>(p, tq, tk, tv, num_sms, stream);
+                       const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs, int D,
+                       int num_sms, cudaStream_t stream) {
+    if (D == 128) return launch_fwd_d<128>(p, tq, tk, tv, tks, tvs, num_sms, stream);
+    if (D == 64) return launch_fwd_d<64>(p, tq, tk, tv, tks, tvs, num_sms, stream);
     return cudaErrorInvalidValue;
 }
 

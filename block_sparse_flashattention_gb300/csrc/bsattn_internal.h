@@ -67,6 +67,15 @@ struct FwdParams {
     int pairs_per_head;            // ceil(total_m / 2)
     int num_units;                 // H * pairs_per_head
     int dynamic;                   // units claimed from sched_order through sched_counter
+    // Proxy compensation (batched): after each unit's listed tiles, summary items
+    // over the KV-tile summaries (mean K, summed V) of the tiles' sequences; a
+    // summary column counts only if its tile is not in the row's exact selection
+    // (sel_words, bit n % 32 of word n / 32), with a denominator mass of 128 keys,
+    // proxy_tail for the sequence's last tile.
+    int proxy;
+    const uint32_t *sel_words;
+    int sel_words_per_row;
+    int proxy_tail;
     uint32_t *sched_counter;       // workspace: next slot of sched_order
     int32_t *sched_order;          // workspace: units, heaviest first
 };
@@ -75,7 +84,10 @@ struct FwdParams {
 constexpr int kMaxScheduledUnits = 98304;
 
 cudaError_t launch_meta(const MetaParams &p, cudaStream_t stream);
+cudaError_t launch_kv_summary(const void *k, const void *v, int B, int S, int H, int D, void *k_sum,
+                              void *v_sum, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                       const CUtensorMap &tv, int D, int num_sms, cudaStream_t stream);
+                       const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs, int D,
+                       int num_sms, cudaStream_t stream);
 
 }  // namespace bsattn

@@ -224,6 +224,11 @@ __device__ __forceinline__ void mbar_arrive_lead(uint32_t lead, uint32_t bar) {
         : "memory");
 }
 
+// One column: lane l of the warp reads TMEM lane (taddr lane + l), column taddr.
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &v) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

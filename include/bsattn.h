@@ -134,6 +134,22 @@ bsattn_status bsattn_build_meta(const uint8_t *block_map, const int32_t *cu_seql
                                 int32_t *err_flag, void *stream);
 
 /*
+ * bsattn_kv_summaries -- per-KV-tile summaries for proxy compensation
+ * ("feat(prims-ts): support proxy-compensated block-sparse attention", FlashInfer
+ * #4872: one arithmetic-mean K summary and one summed-V summary per KV block).
+ * For sequence b, KV tile n and head h, over the keys j of the tile
+ * (128 n <= j < min(128 n + 128, seqlen_k)):
+ *   k_sum[b, n, h, :] = mean_j k[b, j, h, :],   v_sum[b, n, h, :] = sum_j v[b, j, h, :]
+ * accumulated in fp32 in ascending j, rounded to bf16 (round to nearest even).
+ *
+ * k, v          device bf16 [B, seqlen_k, H, D], contiguous, 4-byte aligned.
+ * k_sum, v_sum  device bf16 [B, ceil(seqlen_k / 128), H, D] (written).
+ * D even, at most 256; B, H, seqlen_k > 0.
+ */
+bsattn_status bsattn_kv_summaries(const void *k, const void *v, int32_t B, int32_t seqlen_k,
+                                  int32_t H, int32_t D, void *k_sum, void *v_sum, void *stream);
+
+/*
  * bsattn_build_meta_blocks -- bsattn_build_meta for a block map given at a
  * sparse block size that is a multiple of the 128-token tile ("[CuTe,Flex]
  * varlen blocksparsity", flash-attention #2224: q_subtile_factor; "[feat] VSA-256
@@ -257,6 +273,36 @@ bsattn_status bsattn_fwd(const void *q, const void *k, const void *v, int32_t B,
                          const bsattn_mask_params *mp, float softmax_scale, void *out,
                          bsattn_out_dtype out_dtype, float *lse, void *workspace,
                          size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
+ * bsattn_fwd_proxy -- block-sparse forward with proxy compensation ("feat(prims-ts):
+ * support proxy-compensated block-sparse attention", FlashInfer #4872: selected
+ * blocks stay exact; each omitted KV block is represented by its mean-K and
+ * summed-V summaries, and the softmax denominator counts the block's true number
+ * of keys).  Batched, mask kind none (the page's proxy mode needs a dense mask),
+ * no kv_valid_len.  For query row i of sequence b, head h, Q tile m:
+ *   E = keys j < seqlen_k of the tiles in the lists of (b, h, m)  (exact),
+ *   O = KV tiles n < num_n whose bit is clear in sel_words row (b, h, m) (omitted),
+ *   s_j = scale q_i.k_j,  t_n = scale q_i.k_sum[b, n, h],  w_n = keys of tile n,
+ *   den = sum_E exp(s_j) + sum_O w_n exp(t_n),
+ *   out_i = (sum_E exp(s_j) v_j + sum_O exp(t_n) v_sum[b, n, h]) / den,
+ *   lse_i = ln(den).
+ * The exact lists and sel_words describe the same selection (e.g. lists from
+ * bsattn_build_meta with kind none and the same map, and the bitmask form of that
+ * map); a tile in the lists but not in sel_words would be counted twice.
+ *
+ * sel_words      device uint32 [B * H * num_m][words_per_row], bit n % 32 of word
+ *                n / 32 = tile n is computed exactly; words_per_row >= ceil(num_n / 32).
+ * k_sum, v_sum   device bf16 [B, num_n, H, D], 16-byte aligned (bsattn_kv_summaries).
+ * Other arguments as for bsattn_fwd.  Varlen -> BSATTN_ERR_UNSUPPORTED.
+ */
+bsattn_status bsattn_fwd_proxy(const void *q, const void *k, const void *v, int32_t B,
+                               int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                               const bsattn_meta *meta, const uint32_t *sel_words,
+                               int32_t words_per_row, const void *k_sum, const void *v_sum,
+                               float softmax_scale, void *out, bsattn_out_dtype out_dtype, float *lse,
+                               void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                               void *stream);
 
 /*
  * bsattn_fwd_workspace_size -- bytes of workspace bsattn_fwd can use for this

@@ -300,3 +300,67 @@ def fwd(wl, q, k, v, meta, threads=None):
     o = o.reshape(wl.B, S, wl.H, wl.D)
     lse = lse.reshape(wl.H, wl.B, S).transpose(1, 0, 2)            # [B, H, S]
     return np.ascontiguousarray(o), np.ascontiguousarray(lse)
+
+
+# ---- proxy compensation ("feat(prims-ts): support proxy-compensated block-sparse
+# attention", FlashInfer #4872): selected blocks exact, each omitted KV block
+# represented by its arithmetic-mean K and summed V, the softmax denominator
+# counting the block's true number of keys.  Batched, mask kind none.
+
+def _widen(bits):
+    """bf16 bits -> float64 (exact)."""
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def kv_summaries(wl, k, v):
+    """Per (b, KV tile n, h): mean of the tile's keys and sum of its values over
+    the keys j < seqlen_k, in fp64.  Returns (k_mean, v_sum) [B, num_n, H, D]."""
+    kf, vf = _widen(k), _widen(v)
+    B, S, H, D = kf.shape
+    nn = -(-S // wl.tile_n)
+    km = np.zeros((B, nn, H, D))
+    vs = np.zeros((B, nn, H, D))
+    for n in range(nn):
+        j0, j1 = n * wl.tile_n, min((n + 1) * wl.tile_n, S)
+        km[:, n] = kf[:, j0:j1].mean(axis=1)
+        vs[:, n] = vf[:, j0:j1].sum(axis=1)
+    return km, vs
+
+
+def fwd_proxy(wl, q, k, v, k_sum, v_sum, sel_map):
+    """Proxy-compensated forward, fp64.  sel_map [B, H, num_m, num_n] marks the
+    exactly computed tiles; k_sum / v_sum [B, num_n, H, D] are the summaries the
+    kernel is given (bf16 bits, or float64).  For row i of (b, h): E = keys of the selected
+    tiles below seqlen_k, O = unselected tiles n < num_n with w_n keys each;
+    den = sum_E e^{s_j} + sum_O w_n e^{t_n}, out = (sum_E e^{s_j} v_j +
+    sum_O e^{t_n} v_sum_n) / den, lse = ln den (s_j = scale q.k_j,
+    t_n = scale q.k_sum_n).  Returns O [B, S_q, H, D] and LSE [B, H, S_q]."""
+    qf, kf, vf = _widen(q), _widen(k), _widen(v)
+    # summaries as bf16 bits (what the kernel reads) or as exact float64 values
+    ks = _widen(k_sum) if np.asarray(k_sum).dtype == np.uint16 else np.asarray(k_sum, np.float64)
+    vs = _widen(v_sum) if np.asarray(v_sum).dtype == np.uint16 else np.asarray(v_sum, np.float64)
+    B, Sq, H, D = qf.shape
+    Sk = kf.shape[1]
+    tm, tn = wl.tile_m, wl.tile_n
+    nn = -(-Sk // tn)
+    w = np.array([min(tn, Sk - n * tn) for n in range(nn)], np.float64)
+    out = np.zeros((B, Sq, H, D))
+    lse = np.zeros((B, H, Sq))
+    tile_of_key = np.arange(Sk) // tn
+    for b in range(B):
+        for h in range(H):
+            s = wl.scale * qf[b, :, h] @ kf[b, :, h].T                   # [Sq, Sk]
+            t = wl.scale * qf[b, :, h] @ ks[b, :, h].T                   # [Sq, nn]
+            sel = np.asarray(sel_map[b, h], dtype=bool)                  # [num_m, nn]
+            row_sel = sel[np.arange(Sq) // tm]                           # [Sq, nn]
+            exact = row_sel[:, tile_of_key]                              # [Sq, Sk]
+            s = np.where(exact, s, -np.inf)
+            t = np.where(row_sel, -np.inf, t)
+            m = np.maximum(s.max(axis=1), t.max(axis=1))[:, None]
+            es = np.exp(s - m)
+            et = np.exp(t - m)
+            den = es.sum(axis=1) + (et * w[None]).sum(axis=1)
+            num = es @ vf[b, :, h] + et @ vs[b, :, h]
+            out[b, :, h] = num / den[:, None]
+            lse[b, h] = m[:, 0] + np.log(den)
+    return out, lse

@@ -198,3 +198,34 @@ def test_block_map_entry_point_rejects_bad_arguments(kw, expect):
              mask_params=None, meta=_meta(), err_flag=None, stream=0)
     a.update(kw)
     assert bsa.bsattn_build_meta_blocks(**a) == expect
+
+
+def _prox(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, seqlen_q=256, seqlen_k=256, H=2, D=128, meta=_meta(),
+             sel_words=FAKE, words_per_row=1, k_sum=FAKE, v_sum=FAKE, softmax_scale=0.125,
+             out=FAKE, out_dtype=bsa.OUT_F32, lse=FAKE, workspace=None, workspace_bytes=0,
+             err_flag=None, stream=0)
+    a.update(kw)
+    return bsa.bsattn_fwd_proxy(**a)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(sel_words=None), INV),
+    (dict(k_sum=None), INV),
+    (dict(v_sum=FAKE + 4), INV),                                  # not 16-byte aligned
+    (dict(words_per_row=0), INV),
+    (dict(meta=_meta(num_n=40), seqlen_k=5000), INV),             # 1 word < 40 tiles
+    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), UNS),
+    (dict(D=96), UNS),
+    (dict(softmax_scale=0.0), INV),
+])
+def test_proxy_forward_rejects_bad_arguments(kw, expect):
+    assert _prox(**kw) == expect
+
+
+@pytest.mark.parametrize("kw", [dict(k=None), dict(B=0), dict(D=7), dict(seqlen_k=0),
+                                dict(k_sum=FAKE + 2)])
+def test_kv_summaries_rejects_bad_arguments(kw):
+    a = dict(k=FAKE, v=FAKE, B=1, seqlen_k=256, H=2, D=128, k_sum=FAKE, v_sum=FAKE, stream=0)
+    a.update(kw)
+    assert bsa.bsattn_kv_summaries(**a) == INV
