@@ -364,3 +364,89 @@ def fwd_proxy(wl, q, k, v, k_sum, v_sum, sel_map):
             out[b, :, h] = num / den[:, None]
             lse[b, h] = m[:, 0] + np.log(den)
     return out, lse
+
+
+# ---- backward (the gradients of the forward defined above; batched) ---------
+
+def allowed_mask(wl, meta, b, h):
+    """bool [S_q, S_k]: key j is in query row i's allowed set for (b, h): j in a
+    full-list tile of row i's Q tile and below seqlen_k, or in a mask-list tile and
+    also passing the token predicate and the tile's valid length."""
+    Sq, Sk = int(wl.seqlens_q[b]), int(wl.seqlens_k[b])
+    tm, tn = wl.tile_m, wl.tile_n
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    if wl.kind == 0:
+        pred = np.ones((Sq, Sk), bool)
+    elif wl.kind == 1:
+        pred = j <= i
+    elif wl.kind == 2:
+        pred = (j <= i) & ((i - j < wl.window_left) | (j < wl.sink_tokens))
+    elif wl.kind == 4:
+        pred = (j < wl.prefix_len) | (j <= i)
+    elif wl.kind == 3:
+        dq = np.asarray(wl.doc_id_q)[b * Sq:(b + 1) * Sq]
+        dk = np.asarray(wl.doc_id_k)[b * Sk:(b + 1) * Sk]
+        pred = dq[:, None] == dk[None, :]
+    else:
+        raise ValueError(wl.kind)
+    out = np.zeros((Sq, Sk), bool)
+    for m in range(-(-Sq // tm)):
+        r0, r1 = m * tm, min((m + 1) * tm, Sq)
+        for key, masked in (("full", False), ("mask", True)):
+            cnt = int(meta[key + "_cnt"][b, h, m])
+            for n in meta[key + "_idx"][b, h, m, :cnt]:
+                c0, c1 = int(n) * tn, min((int(n) + 1) * tn, Sk)
+                if c1 <= c0:
+                    continue
+                blk = np.ones((r1 - r0, c1 - c0), bool)
+                if masked:
+                    blk &= pred[r0:r1, c0:c1]
+                    if wl.kv_valid_len is not None:
+                        blk &= (np.arange(c1 - c0) < int(wl.kv_valid_len[b, int(n)]))[None, :]
+                out[r0:r1, c0:c1] |= blk
+    return out
+
+
+def _probs(wl, meta, b, h, qf, kf):
+    A = allowed_mask(wl, meta, b, h)
+    s = np.where(A, wl.scale * qf[b, :, h] @ kf[b, :, h].T, -np.inf)
+    mx = s.max(axis=1, keepdims=True)
+    mx = np.where(np.isfinite(mx), mx, 0.0)
+    e = np.where(A, np.exp(s - mx), 0.0)
+    den = e.sum(axis=1, keepdims=True)
+    return np.divide(e, den, out=np.zeros_like(e), where=den > 0)
+
+
+def fwd_f64(wl, meta, qf, kf, vf):
+    """O = P V over the allowed keys, for float64 inputs [B, S, H, D] (batched)."""
+    out = np.zeros(qf.shape[:3] + (vf.shape[3],))
+    for b in range(wl.B):
+        for h in range(wl.H):
+            out[b, :, h] = _probs(wl, meta, b, h, qf, kf) @ vf[b, :, h]
+    return out
+
+
+def bwd_f64(wl, meta, qf, kf, vf, gf):
+    """Gradients of fwd_f64 for upstream gradient gf (float64, batched):
+    P = softmax over the allowed keys of scale q.k (a row with none has P = 0),
+    O = P V,  dV = P^T dO,  dP = dO V^T,  D_i = sum_d dO_i O_i,
+    dS = P (dP - D),  dQ = scale dS K,  dK = scale dS^T Q."""
+    dq, dk, dv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            P = _probs(wl, meta, b, h, qf, kf)
+            O = P @ vf[b, :, h]
+            g = gf[b, :, h]
+            dv[b, :, h] = P.T @ g
+            dP = g @ vf[b, :, h].T
+            Dv = (g * O).sum(axis=1, keepdims=True)
+            dS = P * (dP - Dv)
+            dq[b, :, h] = wl.scale * dS @ kf[b, :, h]
+            dk[b, :, h] = wl.scale * dS.T @ qf[b, :, h]
+    return dq, dk, dv
+
+
+def bwd(wl, q, k, v, meta, dout):
+    """bwd_f64 on bf16 inputs (raw bits); dQ, dK, dV in the layouts of q, k, v."""
+    return bwd_f64(wl, meta, _widen(q), _widen(k), _widen(v), _widen(dout))

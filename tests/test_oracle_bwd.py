@@ -1,0 +1,76 @@
+"""The oracle's backward pinned to things other than itself: its allowed-key
+masks reproduce the C oracle's forward; its gradients match central finite
+differences of L = sum(O * G); on a dense causal map they match torch autograd
+in fp64."""
+import numpy as np
+import pytest
+
+import oracle
+from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX,
+                               MASK_SLIDING_WINDOW, random_workload)
+
+
+def _w(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+CASES = [
+    dict(seed=201, B=1, H=2, D=16, seqlens_q=[300], seqlens_k=[260], kind=MASK_CAUSAL),
+    dict(seed=202, B=2, H=1, D=8, seqlens_q=[200, 200], kind=MASK_SLIDING_WINDOW, window_left=90,
+         sink_tokens=20, valid_len=True),
+    dict(seed=203, B=1, H=1, D=8, seqlens_q=[256], seqlens_k=[400], kind=MASK_PREFIX,
+         prefix_len=150, valid_len=True),
+    dict(seed=204, B=1, H=2, D=8, seqlens_q=[260], kind=MASK_NONE, density=0.6),
+]
+
+
+@pytest.mark.parametrize("c", CASES)
+def test_allowed_masks_reproduce_the_c_oracle_forward(c):
+    wl = random_workload(**c)
+    q, k, v = wl.qkv()
+    meta = oracle.build_meta(wl)
+    o_c, _ = oracle.fwd(wl, q, k, v, meta)
+    o_np = oracle.fwd_f64(wl, meta, _w(q), _w(k), _w(v))
+    assert np.max(np.abs(o_c - o_np)) < 1e-12
+
+
+@pytest.mark.parametrize("c", CASES[:3])
+def test_gradients_match_finite_differences(c):
+    wl = random_workload(**c)
+    q, k, v = (_w(x) for x in wl.qkv())
+    meta = oracle.build_meta(wl)
+    rng = np.random.default_rng(c["seed"])
+    G = rng.standard_normal(q.shape[:3] + (v.shape[3],))
+    dq, dk, dv = oracle.bwd_f64(wl, meta, q, k, v, G)
+
+    def loss(qq, kk, vv):
+        return float((oracle.fwd_f64(wl, meta, qq, kk, vv) * G).sum())
+
+    eps = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) -
+                  loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_dense_causal_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    wl = random_workload(205, B=1, H=2, D=16, seqlens_q=[256], kind=MASK_CAUSAL, density=1.0)
+    wl.block_map[:] = 1
+    q, k, v = (_w(x) for x in wl.qkv())
+    meta = oracle.build_meta(wl)
+    G = np.random.default_rng(5).standard_normal(q.shape)
+    dq, dk, dv = oracle.bwd_f64(wl, meta, q, k, v, G)
+    tq, tk, tv = (torch.tensor(x.transpose(0, 2, 1, 3), requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=wl.scale)
+    o.backward(torch.tensor(G.transpose(0, 2, 1, 3)))
+    for ref, got in ((tq.grad, dq), (tk.grad, dk), (tv.grad, dv)):
+        assert np.max(np.abs(ref.numpy().transpose(0, 2, 1, 3) - got)) < 1e-10
