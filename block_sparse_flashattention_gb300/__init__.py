@@ -3,9 +3,10 @@
 The compute path is the CUDA library libbsattn.so (include/bsattn.h): a metadata
 kernel that turns a boolean block map into full / mask block lists, and a
 persistent TMA + tcgen05 attention kernel that walks those lists.  This package
-is the Python face of that C ABI: ``bsattn_build_meta`` and ``bsattn_fwd`` carry
-the C names and only marshal arguments; ``alloc_meta``, ``build_meta`` and
-``forward`` add torch allocation of the outputs around them.  PyTorch provides
+is the Python face of that C ABI: ``bsattn_build_meta``, ``bsattn_fwd``,
+``bsattn_bwd`` and the rest carry the C names and only marshal arguments;
+``alloc_meta``, ``build_meta``, ``forward`` and ``backward`` add torch
+allocation of the outputs around them.  PyTorch provides
 device memory and streams only.
 """
 from __future__ import annotations
@@ -19,13 +20,13 @@ from ._binding import (BSATTN_ERR_CAPACITY, BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_
                        OUT_BF16, OUT_F32,
                        BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
                        bsattn_build_meta_bitmask, bsattn_build_meta_blocks, bsattn_build_meta_bsr,
-                       bsattn_fwd_proxy, bsattn_kv_summaries,
+                       bsattn_fwd_proxy, bsattn_kv_summaries, bsattn_bwd, bsattn_bwd_workspace_size,
                        bsattn_fwd, bsattn_fwd_static_scratch, bsattn_fwd_workspace_size, library,
                        status_string)
 
 TILE = 128
 
-__all__ = ["bsattn_fwd_proxy", "bsattn_kv_summaries", "bsattn_build_meta", "bsattn_build_meta_bitmask", "bsattn_build_meta_blocks", "bsattn_build_meta_bsr", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version",
+__all__ = ["bsattn_bwd", "bsattn_bwd_workspace_size", "backward", "bsattn_fwd_proxy", "bsattn_kv_summaries", "bsattn_build_meta", "bsattn_build_meta_bitmask", "bsattn_build_meta_blocks", "bsattn_build_meta_bsr", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version",
            "alloc_meta", "alloc_workspace", "build_meta",
            "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
            "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
@@ -126,3 +127,37 @@ def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_val
                       err_flag=err_flag, stream=stream),
            "bsattn_fwd")
     return out, lse
+
+
+def backward(q, k, v, out, lse, dout, meta: Meta, *, kv_valid_len=None, kind: int = MASK_NONE,
+             mask_params: Optional[MaskParams] = None, softmax_scale: Optional[float] = None,
+             grad_dtype=None, workspace=None, err_flag=None, stream=None):
+    """Gradients (dq, dk, dv) of ``forward`` (batched) for upstream gradient dout.
+
+    q/k/v/dout: bf16 [B, S, H, D]; out, lse: the forward's results for the same
+    arguments.  Gradients are bf16 by default, or torch.float32.  workspace: a
+    uint8 tensor of at least bsattn_bwd_workspace_size(meta) bytes, or None to
+    allocate one for this call."""
+    import torch
+    if meta.varlen:
+        raise BsattnError(BSATTN_ERR_UNSUPPORTED, "backward (varlen)")
+    B, seqlen_q, H, D = q.shape
+    seqlen_k = k.shape[1]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if grad_dtype is None:
+        grad_dtype = torch.bfloat16
+    if grad_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("grad_dtype must be torch.bfloat16 or torch.float32")
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(bsattn_bwd_workspace_size(meta), dtype=torch.uint8, device=q.device)
+    gd = OUT_F32 if grad_dtype == torch.float32 else OUT_BF16
+    od = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(bsattn_bwd(q, k, v, out, od, lse, dout, B, seqlen_q, seqlen_k, H, D, meta, kv_valid_len,
+                      kind, mask_params, softmax_scale, dq, dk, dv, gd, workspace,
+                      err_flag=err_flag, stream=stream),
+           "bsattn_bwd")
+    return dq, dk, dv

@@ -96,6 +96,17 @@ def library() -> ctypes.CDLL:
         lib.bsattn_fwd_workspace_size.argtypes = [ctypes.POINTER(bsattn_meta),
                                                   ctypes.POINTER(ctypes.c_size_t)]
         lib.bsattn_fwd_workspace_size.restype = ctypes.c_int
+        lib.bsattn_bwd.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(bsattn_meta), ctypes.c_void_p,
+            ctypes.c_int, ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+            ctypes.c_void_p, ctypes.c_void_p]
+        lib.bsattn_bwd.restype = ctypes.c_int
+        lib.bsattn_bwd_workspace_size.argtypes = [ctypes.POINTER(bsattn_meta),
+                                                  ctypes.POINTER(ctypes.c_size_t)]
+        lib.bsattn_bwd_workspace_size.restype = ctypes.c_int
         lib.bsattn_status_string.argtypes = [ctypes.c_int]
         lib.bsattn_status_string.restype = ctypes.c_char_p
         lib.bsattn_abi_version.argtypes = []
@@ -280,6 +291,34 @@ def bsattn_fwd_workspace_size(meta: Meta) -> int:
     st = library().bsattn_fwd_workspace_size(ctypes.byref(mt), ctypes.byref(n))
     if st != BSATTN_OK:
         raise BsattnError(st, "bsattn_fwd_workspace_size")
+    return int(n.value)
+
+
+def bsattn_bwd(q, k, v, out, out_dtype: int, lse, dout, B: int, seqlen_q: int, seqlen_k: int,
+               H: int, D: int, meta: Meta, kv_valid_len, kind: int,
+               mask_params: Optional[MaskParams], softmax_scale: float, dq, dk, dv,
+               grad_dtype: int, workspace, workspace_bytes: int = 0, err_flag=None,
+               stream=None) -> int:
+    """Forwards to the C function of the same name; returns its status code."""
+    mp = mask_params.to_c() if mask_params is not None else None
+    mt = meta.to_c()
+    if workspace is not None and not isinstance(workspace, int) and workspace_bytes == 0:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    return library().bsattn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(out_dtype), _ptr(lse), _ptr(dout), int(B),
+        int(seqlen_q), int(seqlen_k), int(H), int(D), ctypes.byref(mt), _ptr(kv_valid_len),
+        int(kind), ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(dq),
+        _ptr(dk), _ptr(dv), int(grad_dtype), _ptr(workspace), int(workspace_bytes),
+        _ptr(err_flag), _stream(stream))
+
+
+def bsattn_bwd_workspace_size(meta: Meta) -> int:
+    """Bytes of workspace bsattn_bwd needs for `meta` (batched)."""
+    mt = meta.to_c()
+    n = ctypes.c_size_t(0)
+    st = library().bsattn_bwd_workspace_size(ctypes.byref(mt), ctypes.byref(n))
+    if st != BSATTN_OK:
+        raise BsattnError(st, "bsattn_bwd_workspace_size")
     return int(n.value)
 
 

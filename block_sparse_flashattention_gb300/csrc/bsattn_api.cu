@@ -266,6 +266,30 @@ bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, i
     return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
 }
 
+// Workspace of bsattn_bwd, in 256-byte aligned regions: the KV-major counts
+// (full, mask) [B, H, num_n], the KV-major lists (full, mask) [B, H, num_n,
+// num_m], then LSE * log2(e) and D, fp32 [B * H][num_m * 128] each.
+struct BwdLayout {
+    size_t t_full_cnt, t_mask_cnt, t_full_idx, t_mask_idx, lse2, dvec, total;
+};
+
+BwdLayout bwd_layout(const bsattn_meta *m) {
+    auto up = [](size_t x) { return (x + 255u) & ~(size_t)255u; };
+    const size_t bh = (size_t)m->B * (size_t)m->H;
+    const size_t cnt = up(bh * (size_t)m->num_n * 4u);
+    const size_t idx = up(bh * (size_t)m->num_n * (size_t)m->num_m * 4u);
+    const size_t row = up(bh * (size_t)m->num_m * (size_t)kTile * 4u);
+    BwdLayout L;
+    L.t_full_cnt = 0;
+    L.t_mask_cnt = L.t_full_cnt + cnt;
+    L.t_full_idx = L.t_mask_cnt + cnt;
+    L.t_mask_idx = L.t_full_idx + idx;
+    L.lse2 = L.t_mask_idx + idx;
+    L.dvec = L.lse2 + row;
+    L.total = L.dvec + row;
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -413,6 +437,102 @@ bsattn_status bsattn_fwd_proxy(const void *q, const void *k, const void *v, int3
     return fwd_impl(q, k, v, B, seqlen_q, seqlen_k, H, D, nullptr, nullptr, meta, nullptr,
                     BSATTN_MASK_NONE, nullptr, softmax_scale, out, out_dtype, lse, workspace,
                     workspace_bytes, err_flag, stream, &pa);
+}
+
+bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    if (!bytes) return BSATTN_ERR_INVALID_ARG;
+    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;
+    *bytes = bwd_layout(meta).total;
+    return BSATTN_OK;
+}
+
+bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void *out,
+                         bsattn_out_dtype out_dtype, const float *lse, const void *dout, int32_t B,
+                         int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                         const bsattn_meta *meta, const int32_t *kv_valid_len, bsattn_mask_kind kind,
+                         const bsattn_mask_params *mp, float softmax_scale, void *dq, void *dk, void *dv,
+                         bsattn_out_dtype grad_dtype, void *workspace, size_t workspace_bytes,
+                         int32_t *err_flag, void *stream) {
+    bsattn_status st = check_meta(meta);
+    if (st != BSATTN_OK) return st;
+    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched only
+    if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
+        return BSATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return BSATTN_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
+    if (meta->B != B || meta->H != H) return BSATTN_ERR_INVALID_ARG;
+    if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+        return BSATTN_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSATTN_ERR_INVALID_ARG;
+    if (out_dtype != BSATTN_OUT_BF16 && out_dtype != BSATTN_OUT_F32) return BSATTN_ERR_INVALID_ARG;
+    if (grad_dtype != BSATTN_OUT_BF16 && grad_dtype != BSATTN_OUT_F32) return BSATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+    const long long rows_q = (long long)B * seqlen_q, rows_k = (long long)B * seqlen_k;
+    if (rows_q > INT32_MAX || rows_k > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+    const BwdLayout L = bwd_layout(meta);
+    if (workspace_bytes < L.total) return BSATTN_ERR_INVALID_ARG;
+    if (rows_q == 0 || rows_k == 0) {
+        // no keys (every row's key set is empty) or no queries: all gradients are 0
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const size_t el = grad_dtype == BSATTN_OUT_F32 ? 4u : 2u;
+        if (cudaMemsetAsync(dq, 0, (size_t)rows_q * H * D * el, s) != cudaSuccess ||
+            cudaMemsetAsync(dk, 0, (size_t)rows_k * H * D * el, s) != cudaSuccess ||
+            cudaMemsetAsync(dv, 0, (size_t)rows_k * H * D * el, s) != cudaSuccess)
+            return BSATTN_ERR_CUDA;
+        return BSATTN_OK;
+    }
+
+    char *ws = static_cast<char *>(workspace);
+    bsattn::BwdParams p = {};
+    p.B = B;
+    p.H = H;
+    p.D = D;
+    p.seqlen_q = seqlen_q;
+    p.seqlen_k = seqlen_k;
+    p.num_m = meta->num_m;
+    p.num_n = meta->num_n;
+    p.scale = softmax_scale;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
+    p.full_cnt = meta->full_cnt;
+    p.full_idx = meta->full_idx;
+    p.mask_cnt = meta->mask_cnt;
+    p.mask_idx = meta->mask_idx;
+    p.t_full_cnt = reinterpret_cast<int32_t *>(ws + L.t_full_cnt);
+    p.t_mask_cnt = reinterpret_cast<int32_t *>(ws + L.t_mask_cnt);
+    p.t_full_idx = reinterpret_cast<int32_t *>(ws + L.t_full_idx);
+    p.t_mask_idx = reinterpret_cast<int32_t *>(ws + L.t_mask_idx);
+    p.vl = kv_valid_len;
+    p.kind = (int)kind;
+    if (mp) {
+        p.window_left = mp->window_left;
+        p.sink_tokens = mp->sink_tokens;
+        p.prefix_len = mp->prefix_len;
+        p.doc_q = mp->doc_id_q;
+        p.doc_k = mp->doc_id_k;
+    }
+    p.o = out;
+    p.o_f32 = out_dtype == BSATTN_OUT_F32 ? 1 : 0;
+    p.dout = static_cast<const uint16_t *>(dout);
+    p.lse = lse;
+    p.lse2 = reinterpret_cast<float *>(ws + L.lse2);
+    p.dvec = reinterpret_cast<float *>(ws + L.dvec);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.grad_f32 = grad_dtype == BSATTN_OUT_F32 ? 1 : 0;
+    p.err = err_flag;
+
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_bshd(&tq, q, rows_q, H, D) || !encode_bshd(&tk, k, rows_k, H, D) ||
+        !encode_bshd(&tv, v, rows_k, H, D) || !encode_bshd(&tdo, dout, rows_q, H, D))
+        return BSATTN_ERR_CUDA;
+    cudaError_t e = bsattn::launch_bwd(p, tq, tk, tv, tdo, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSATTN_OK : BSATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -83,6 +83,29 @@ struct FwdParams {
 // Units the scheduling pass can order (its per-unit keys live in shared memory).
 constexpr int kMaxScheduledUnits = 98304;
 
+// Backward (batched): dK/dV per KV tile over the KV-major lists, dQ per Q tile
+// over the forward lists.
+struct BwdParams {
+    int B, H, D, seqlen_q, seqlen_k, num_m, num_n;
+    float scale, scale_log2;
+    const int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;  // forward lists
+    int32_t *t_full_cnt, *t_full_idx, *t_mask_cnt, *t_mask_idx; // KV-major: [B, H, num_n(, num_m)]
+    const int32_t *vl;            // [B, num_n] or null (mask tiles only)
+    int kind, window_left, sink_tokens, prefix_len;
+    const int32_t *doc_q, *doc_k;
+    const void *o;                // forward output, bf16 or fp32 ([B, S_q, H, D])
+    int o_f32;
+    const uint16_t *dout;         // bf16 [B, S_q, H, D]
+    const float *lse;             // [B, H, S_q], natural log
+    float *lse2, *dvec;           // workspace [B * H][num_m * 128]: LSE * log2(e), D
+    void *dq, *dk, *dv;           // gradients in q / k / v layouts
+    int grad_f32;
+    int32_t *err;
+};
+
+cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream);
+
 cudaError_t launch_meta(const MetaParams &p, cudaStream_t stream);
 cudaError_t launch_kv_summary(const void *k, const void *v, int B, int S, int H, int D, void *k_sum,
                               void *v_sum, cudaStream_t stream);

@@ -229,3 +229,48 @@ def test_kv_summaries_rejects_bad_arguments(kw):
     a = dict(k=FAKE, v=FAKE, B=1, seqlen_k=256, H=2, D=128, k_sum=FAKE, v_sum=FAKE, stream=0)
     a.update(kw)
     assert bsa.bsattn_kv_summaries(**a) == INV
+
+
+def _bwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, out_dtype=bsa.OUT_F32, lse=FAKE, dout=FAKE, B=1,
+             seqlen_q=256, seqlen_k=256, H=2, D=128, meta=_meta(), kv_valid_len=None,
+             kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, dq=FAKE, dk=FAKE,
+             dv=FAKE, grad_dtype=bsa.OUT_F32, workspace=FAKE, workspace_bytes=1 << 20,
+             err_flag=None, stream=0)
+    a.update(kw)
+    return bsa.bsattn_bwd(**a)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(D=96), UNS),
+    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), UNS),
+    (dict(dout=None), INV),
+    (dict(lse=None), INV),
+    (dict(dq=FAKE + 2), INV),                                  # not 16-byte aligned
+    (dict(dv=None), INV),
+    (dict(workspace=None), INV),
+    (dict(workspace=FAKE + 16), INV),                          # not 256-byte aligned
+    (dict(workspace_bytes=16), INV),                           # too small
+    (dict(grad_dtype=5), INV),
+    (dict(out_dtype=9), INV),
+    (dict(seqlen_k=300), INV),                                 # num_n would be 3
+    (dict(B=2), INV),
+    (dict(kind=bsa.MASK_SLIDING_WINDOW), INV),
+    (dict(softmax_scale=0.0), INV),
+    (dict(meta=_meta(tile_n=64)), UNS),
+])
+def test_bwd_rejects_bad_arguments(kw, expect):
+    assert _bwd(**kw) == expect
+
+
+def test_bwd_workspace_size():
+    # counts 2 x [B*H*num_n] int32, lists 2 x [B*H*num_n*num_m] int32, rows 2 x
+    # [B*H*num_m*128] fp32, each region rounded up to 256 bytes
+    up = lambda x: -(-x // 256) * 256  # noqa: E731
+    assert bsa.bsattn_bwd_workspace_size(_meta()) == 2 * 256 + 2 * 256 + 2 * 2048
+    m = _meta(B=3, H=5, num_m=7, num_n=9)
+    assert bsa.bsattn_bwd_workspace_size(m) == (2 * up(4 * 135) + 2 * up(4 * 135 * 7)
+                                                + 2 * up(4 * 105 * 128))
+    with pytest.raises(bsa.BsattnError):
+        bsa.bsattn_bwd_workspace_size(_meta(varlen=1, cu_total_m_blocks=FAKE,
+                                            cu_block_idx_offsets=FAKE))

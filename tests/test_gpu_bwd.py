@@ -1,0 +1,158 @@
+"""Backward of the block-sparse forward against the oracle's fp64 gradients.
+
+The step the pages list as missing for training ("[CuTe,Flex] varlen
+blocksparsity", flash-attention #2224; "[feat] VSA-256 fastpath", FastVideo
+#1354).  The CUDA path rounds P and dS to bf16 before their tensor-core
+products (fp32 accumulation) and takes D from the forward's fp32 output, so
+each gradient tensor G is held to
+    max |G - G_ref| <= 2e-2 * max |G_ref|   and   ||G - G_ref||_F <= 1e-2 ||G_ref||_F
+(bf16 carries 8 significant bits: one rounding of P and one of dS each
+contribute a relative error of at most 2^-9 per term).  Gradients in bf16 equal
+the fp32 gradients rounded to nearest even, bit for bit; two runs agree bit for
+bit; rows and keys outside every selected block get exactly 0."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import block_sparse_flashattention_gb300 as bsa  # noqa: E402
+import oracle  # noqa: E402
+from tests.gpu_run import DeviceWorkload, bf16_to_device  # noqa: E402
+from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX,  # noqa: E402
+                               MASK_SLIDING_WINDOW, random_workload)
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL, FRO_TOL = 2e-2, 1e-2
+
+CASES = [
+    dict(seed=301, B=1, H=2, D=64, seqlens_q=[256], kind=MASK_CAUSAL, density=0.5),
+    dict(seed=302, B=2, H=2, D=128, seqlens_q=[300] * 2, seqlens_k=[520] * 2, kind=MASK_CAUSAL,
+         density=0.6),
+    dict(seed=303, B=1, H=2, D=128, seqlens_q=[384], kind=MASK_SLIDING_WINDOW, window_left=150,
+         sink_tokens=40, density=0.7, valid_len=True),
+    dict(seed=304, B=2, H=1, D=64, seqlens_q=[260] * 2, seqlens_k=[400] * 2, kind=MASK_PREFIX,
+         prefix_len=170, density=0.6, valid_len=True),
+    dict(seed=305, B=1, H=3, D=128, seqlens_q=[333], kind=MASK_DOCUMENT, density=0.8),
+    dict(seed=306, B=1, H=2, D=64, seqlens_q=[512], seqlens_k=[700], kind=MASK_NONE,
+         density=0.4, force_diag=False, clear=(1, 2)),     # an empty Q tile and KV tile
+    dict(seed=307, B=1, H=1, D=128, seqlens_q=[1100], kind=MASK_NONE, density=0.9),
+]
+
+
+def _workload(c):
+    c = dict(c)
+    clear = c.pop("clear", None)
+    wl = random_workload(**c)
+    if clear is not None:  # (Q tile, KV tile): that map row and column unselected
+        wl.block_map[:, :, clear[0], :] = 0
+        wl.block_map[:, :, :, clear[1]] = 0
+    return wl
+
+
+def _run(c, out_dtype=torch.float32, grad_dtype=torch.float32):
+    wl = _workload(c)
+    dw = DeviceWorkload(wl, "cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    meta = dw.build_meta(err_flag=err)
+    out, lse = dw.forward(meta, err_flag=err, out_dtype=out_dtype)
+    dout_bits = wl.tensor("do")
+    dout = bf16_to_device(dout_bits, "cuda")
+    dq, dk, dv = bsa.backward(dw.q, dw.k, dw.v, out, lse, dout, meta, kv_valid_len=dw.vl,
+                              kind=wl.kind, mask_params=dw.mask_params, softmax_scale=wl.scale,
+                              grad_dtype=grad_dtype, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return wl, dout_bits, (dq, dk, dv)
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("idx", range(len(CASES)))
+def test_backward_matches_oracle(idx):
+    wl, dout_bits, grads = _run(CASES[idx])
+    q, k, v = wl.qkv()
+    ref = oracle.bwd(wl, q, k, v, oracle.build_meta(wl), dout_bits)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = _f64(g)
+        scale = max(np.max(np.abs(r)), 1e-30)
+        assert np.max(np.abs(g - r)) <= MAX_TOL * scale, name
+        assert np.linalg.norm(g - r) <= FRO_TOL * max(np.linalg.norm(r), 1e-30), name
+
+
+def test_zero_rows_and_keys_outside_the_selection():
+    c = CASES[5]
+    wl, _, (dq, dk, dv) = _run(c)
+    meta = oracle.build_meta(wl)
+    sel_q = (meta["full_cnt"] + meta["mask_cnt"]) > 0          # [B, H, num_m]
+    sel_k = np.zeros((wl.B, wl.H, wl.num_n), bool)
+    for key in ("full", "mask"):
+        for b in range(wl.B):
+            for h in range(wl.H):
+                for m in range(wl.num_m):
+                    sel_k[b, h, meta[key + "_idx"][b, h, m, :meta[key + "_cnt"][b, h, m]]] = True
+    assert (~sel_q).any() and (~sel_k).any()
+    dq, dk, dv = _f64(dq), _f64(dk), _f64(dv)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            for m in np.nonzero(~sel_q[b, h])[0]:
+                assert np.all(dq[b, m * 128:(m + 1) * 128, h] == 0)
+            for n in np.nonzero(~sel_k[b, h])[0]:
+                assert np.all(dk[b, n * 128:(n + 1) * 128, h] == 0)
+                assert np.all(dv[b, n * 128:(n + 1) * 128, h] == 0)
+
+
+@pytest.mark.parametrize("idx", [1, 3])
+def test_bf16_gradients_are_rounded_fp32_gradients(idx):
+    _, _, g32 = _run(CASES[idx])
+    _, _, g16 = _run(CASES[idx], grad_dtype=torch.bfloat16)
+    for a, b in zip(g32, g16):
+        assert torch.equal(a.to(torch.bfloat16), b)
+
+
+def test_deterministic():
+    _, _, g1 = _run(CASES[2])
+    _, _, g2 = _run(CASES[2])
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_bf16_forward_output_is_accepted():
+    wl, dout_bits, grads = _run(CASES[0], out_dtype=torch.bfloat16)
+    q, k, v = wl.qkv()
+    ref = oracle.bwd(wl, q, k, v, oracle.build_meta(wl), dout_bits)
+    for g, r in zip(grads, ref):
+        g = _f64(g)
+        assert np.max(np.abs(g - r)) <= MAX_TOL * np.max(np.abs(r))
+
+
+def test_bad_list_entry_is_flagged_and_skipped():
+    c = CASES[0]
+    wl = _workload(c)
+    dw = DeviceWorkload(wl, "cuda")
+    meta = dw.build_meta()
+    out, lse = dw.forward(meta, out_dtype=torch.float32)
+    dout = bf16_to_device(wl.tensor("do"), "cuda")
+    # an out-of-range entry past a real one: the forward would flag it too, so
+    # only the backward runs on the edited lists
+    cnt = meta.full_cnt.clone()
+    idx = meta.full_idx.clone()
+    b, h, m = 0, 0, 1
+    n = int(cnt[b, h, m])
+    idx[b, h, m, n] = 999
+    cnt[b, h, m] = n + 1
+    bad = bsa.Meta(full_cnt=cnt, full_idx=idx, mask_cnt=meta.mask_cnt, mask_idx=meta.mask_idx,
+                   varlen=0, B=meta.B, H=meta.H, num_m=meta.num_m, num_n=meta.num_n)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g_bad = bsa.backward(dw.q, dw.k, dw.v, out, lse, dout, bad, kind=wl.kind,
+                         mask_params=dw.mask_params, softmax_scale=wl.scale,
+                         grad_dtype=torch.float32, err_flag=err)
+    g_ok = bsa.backward(dw.q, dw.k, dw.v, out, lse, dout, meta, kind=wl.kind,
+                        mask_params=dw.mask_params, softmax_scale=wl.scale,
+                        grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bsa.FLAG_BAD_INDEX
+    for a, b2 in zip(g_bad, g_ok):
+        assert torch.equal(a, b2)

@@ -26,7 +26,7 @@ TILE = 128
 # Mask kinds, numbered as in the C ABI (include/bsattn.h).
 MASK_NONE, MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 0, 1, 2, 3, 4
 
-S_Q, S_K, S_V, S_MAP, S_LEN, S_SCORE, S_VALID, S_DOC = range(8)
+S_Q, S_K, S_V, S_MAP, S_LEN, S_SCORE, S_VALID, S_DOC, S_DO = range(9)
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -105,14 +105,15 @@ class Workload:
         return (self.B, int(self.seqlens_k[0]), self.H, self.D)
 
     def fill(self, which: str, ptr: int) -> None:
-        """Write the bf16 bits of tensor `which` ('q', 'k' or 'v') to host memory at ptr."""
+        """Write the bf16 bits of tensor `which` ('q', 'k', 'v', or 'do': the
+        upstream gradient of the output, shaped like q) to host memory at ptr."""
         from . import normal_bf16_into
-        stream = {"q": S_Q, "k": S_K, "v": S_V}[which]
-        shape = self.q_shape() if which == "q" else self.k_shape()
+        stream = {"q": S_Q, "k": S_K, "v": S_V, "do": S_DO}[which]
+        shape = self.q_shape() if which in ("q", "do") else self.k_shape()
         normal_bf16_into(ptr, int(np.prod(shape)), self.data_seed, stream)
 
     def tensor(self, which: str) -> np.ndarray:
-        shape = self.q_shape() if which == "q" else self.k_shape()
+        shape = self.q_shape() if which in ("q", "do") else self.k_shape()
         out = np.empty(shape, dtype=np.uint16)
         self.fill(which, out.ctypes.data)
         return out
