@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-meta-formats", action="store_true",
                     help="skip the side measurements (metadata formats, proxy A/B)")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward timing")
     ap.add_argument("--heads", type=int, default=0,
                     help="keep only the first N heads (a smaller case for profiling)")
     return ap.parse_args()
@@ -323,6 +324,53 @@ def time_proxy(wl, dw, err, stream, iters=10):
     return res
 
 
+def time_bwd(wl, dw, meta, out, lse, err, stream, flop_fwd, iters=5):
+    """Backward (bsattn_bwd: list transpose, row pass, dK/dV kernel, dQ kernel) on
+    the benchmark's metadata and forward results, with a seeded upstream gradient.
+    Effective TFLOP/s counts 2.5x the forward's FLOPs per computed block (the five
+    128x128xD products S, dP, dV, dK, dQ), the usual attention-backward
+    convention; the kernels recompute S and dP once more (seven products)."""
+    import torch
+    import block_sparse_flashattention_gb300 as bsa
+    if wl.varlen:
+        return {"note": "varlen backward not provided (batched only)"}
+    dev = dw.q.device
+    sq, sk = dw.seqlens()
+    hdo = torch.empty(wl.q_shape(), dtype=torch.int16, pin_memory=True)
+    wl.fill("do", hdo.data_ptr())
+    dout = hdo.to(dev).view(torch.bfloat16)
+    dq = torch.empty_like(dw.q)
+    dk = torch.empty_like(dw.k)
+    dv = torch.empty_like(dw.v)
+    wsb = torch.empty(bsa.bsattn_bwd_workspace_size(meta), dtype=torch.uint8, device=dev)
+
+    def bwd():
+        st = bsa.bsattn_bwd(dw.q, dw.k, dw.v, out, bsa.OUT_BF16, lse, dout, wl.B, sq, sk, wl.H,
+                            wl.D, meta, dw.vl, wl.kind, dw.mask_params, wl.scale, dq, dk, dv,
+                            bsa.OUT_BF16, wsb, err_flag=err, stream=stream.cuda_stream)
+        if st != bsa.BSATTN_OK:
+            raise RuntimeError(bsa.status_string(st))
+
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bwd()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms.append(a.elapsed_time(b))
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())} in the backward")
+    mean = statistics.mean(ms)
+    flop = 2.5 * flop_fwd
+    return {"ms": mean, "tflops": flop / (mean * 1e-3) / 1e12, "flop": flop,
+            "launches_per_call": 4, "grad_dtype": "bf16",
+            "note": "flop = 2.5 x forward flop over computed blocks; events around each call"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -491,6 +539,7 @@ def run_native(args):
         raise RuntimeError(f"device error flag {int(err.item())}")
     meta_formats = time_meta_formats(wl, dw, meta, err, stream) if not args.no_meta_formats else None
     proxy_ab = time_proxy(wl, dw, err, stream) if not args.no_meta_formats else None
+    bwd = time_bwd(wl, dw, meta, out, lse, err, stream, flop_step) if not args.no_bwd else None
 
     if rank != 0:
         if pg:
@@ -545,6 +594,7 @@ def run_native(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / K},
         "meta_formats": meta_formats,
         "proxy_ab": proxy_ab,
+        "bwd": bwd if bwd is None or "ms" not in bwd else dict(bwd, frac=bwd["tflops"] / peak),
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }
