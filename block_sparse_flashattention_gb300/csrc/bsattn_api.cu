@@ -268,9 +268,11 @@ bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, i
 
 // Workspace of bsattn_bwd, in 256-byte aligned regions: the KV-major counts
 // (full, mask) [B, H, num_n], the KV-major lists (full, mask) [B, H, num_n,
-// num_m], then LSE * log2(e) and D, fp32 [B * H][num_m * 128] each.
+// num_m], the 2-bit selection matrix [B, H, num_n][ceil(num_m / 16)] uint32, the
+// KV tile order [B * H * num_n], then LSE * log2(e) and D, fp32 [B * H][num_m *
+// 128] each.
 struct BwdLayout {
-    size_t t_full_cnt, t_mask_cnt, t_full_idx, t_mask_idx, lse2, dvec, total;
+    size_t t_full_cnt, t_mask_cnt, t_full_idx, t_mask_idx, tbits, order, lse2, dvec, total;
 };
 
 BwdLayout bwd_layout(const bsattn_meta *m) {
@@ -278,13 +280,16 @@ BwdLayout bwd_layout(const bsattn_meta *m) {
     const size_t bh = (size_t)m->B * (size_t)m->H;
     const size_t cnt = up(bh * (size_t)m->num_n * 4u);
     const size_t idx = up(bh * (size_t)m->num_n * (size_t)m->num_m * 4u);
+    const size_t bits = up(bh * (size_t)m->num_n * (size_t)((m->num_m + 15) / 16) * 4u);
     const size_t row = up(bh * (size_t)m->num_m * (size_t)kTile * 4u);
     BwdLayout L;
     L.t_full_cnt = 0;
     L.t_mask_cnt = L.t_full_cnt + cnt;
     L.t_full_idx = L.t_mask_cnt + cnt;
     L.t_mask_idx = L.t_full_idx + idx;
-    L.lse2 = L.t_mask_idx + idx;
+    L.tbits = L.t_mask_idx + idx;
+    L.order = L.tbits + bits;
+    L.lse2 = L.order + cnt;
     L.dvec = L.lse2 + row;
     L.total = L.dvec + row;
     return L;
@@ -506,6 +511,9 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
     p.t_mask_cnt = reinterpret_cast<int32_t *>(ws + L.t_mask_cnt);
     p.t_full_idx = reinterpret_cast<int32_t *>(ws + L.t_full_idx);
     p.t_mask_idx = reinterpret_cast<int32_t *>(ws + L.t_mask_idx);
+    p.tbits = reinterpret_cast<uint32_t *>(ws + L.tbits);
+    p.tbits_words = (int)((meta->num_m + 15) / 16);
+    p.order = reinterpret_cast<int32_t *>(ws + L.order);
     p.vl = kv_valid_len;
     p.kind = (int)kind;
     if (mp) {

@@ -6,14 +6,22 @@
 // Training needs the backward, which the pages list as missing ("[CuTe,Flex]
 // varlen blocksparsity", flash-attention #2224; "[feat] VSA-256 fastpath",
 // FastVideo #1354).  It runs as
-//   1. a transpose of the forward's lists into KV-major lists (for each KV tile,
-//      the Q tiles that selected it, full and mask separately, descending);
-//   2. a row pass writing D and LSE * log2(e) into padded per-(b, h) rows;
-//   3. the dK / dV kernel: one CTA per KV tile, S^T = K Q^T and dP^T = V dO^T per
+//   1. list transpose: the forward's (Q tile -> KV tiles) lists are scattered
+//      into a 2-bit matrix per KV tile (none / full / mask for every Q tile),
+//      then one warp per KV tile compacts its column into KV-major lists, Q
+//      tiles in descending order;
+//   2. an order pass: KV tiles sorted by list length, longest first, so the
+//      dK / dV grid starts its longest CTAs first;
+//   3. a row pass writing D and LSE * log2(e) into padded per-(b, h) rows;
+//   4. the dK / dV kernel: one CTA per KV tile, S^T = K Q^T and dP^T = V dO^T per
 //      listed Q tile on tcgen05, P^T and dS^T formed per key row in TMEM, then
-//      dV += P^T dO and dK += dS^T Q accumulated in TMEM;
-//   4. the dQ kernel: one CTA per Q tile, S = Q K^T and dP = dO V^T per listed KV
-//      tile, dS per query row, dQ += dS K accumulated in TMEM.
+//      dV += P^T dO and dK += dS^T Q accumulated in TMEM, handed over in two
+//      halves of the Q tile so that the products of one half overlap the
+//      elementwise work of the other;
+//   5. the dQ kernel: one CTA per Q tile, S = Q K^T and dP = dO V^T per listed KV
+//      tile, dS per query row into one of two TMEM buffers, dQ += dS K
+//      accumulated in TMEM; the next tile's S and dP are issued before this
+//      tile's dQ product, so the elementwise work overlaps it.
 // P is recomputed from the forward's LSE (no running maximum) and rounded to
 // bf16 before the P^T dO product, as the forward rounds it before P V; dS is
 // rounded to bf16 before its products.
@@ -26,56 +34,119 @@ namespace bsattn {
 
 namespace {
 
-// ------------------------------------------------------------ 1. transpose --
-// One CTA per (b, h): Q-tile rows are taken from the last to the first, each
-// row's entries appended to their KV tile's list, so every KV-major list is
-// descending in m.  Entries outside [0, num_n) are skipped and flagged.
-__global__ void __launch_bounds__(256) bsattn_bwd_transpose_kernel(BwdParams p) {
-    const int bh = blockIdx.x;
-    const long long crow = (long long)bh * p.num_n;  // first KV-major count of (b, h)
-    for (int n = threadIdx.x; n < p.num_n; n += blockDim.x) {
-        p.t_full_cnt[crow + n] = 0;
-        p.t_mask_cnt[crow + n] = 0;
-    }
-    __syncthreads();
+// ------------------------------------------------------- 1. list transpose --
+// One warp per forward list row (b, h, m): every valid entry n sets code 1
+// (full) or 2 (mask) for Q tile m in the 2-bit column of KV tile n.  A count
+// outside [0, num_n], an index outside [0, num_n) or a tile listed twice sets
+// BSATTN_FLAG_BAD_INDEX; the bad entry is skipped (a repeat keeps the OR of the
+// codes, so a tile in both lists is treated as a mask tile).
+__global__ void __launch_bounds__(256) bsattn_bwd_scatter_kernel(BwdParams p) {
+    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= (long long)p.B * p.H * p.num_m) return;
+    const long long bh = w / p.num_m;
+    const int m = (int)(w - bh * p.num_m);
     bool bad = false;
-    for (int m = p.num_m - 1; m >= 0; --m) {
-        const long long r = (long long)bh * p.num_m + m;
-        for (int list = 0; list < 2; ++list) {
-            const int32_t *cnt_in = list ? p.mask_cnt : p.full_cnt;
-            const int32_t *idx_in = list ? p.mask_idx : p.full_idx;
-            int32_t *cnt_out = list ? p.t_mask_cnt : p.t_full_cnt;
-            int32_t *idx_out = list ? p.t_mask_idx : p.t_full_idx;
-            int c = cnt_in[r];
-            if (c < 0 || c > p.num_n) {
-                bad = true;
-                c = c < 0 ? 0 : p.num_n;
-            }
-            for (int e = threadIdx.x; e < c; e += blockDim.x) {
-                const int n = idx_in[r * p.num_n + e];
-                if (n < 0 || n >= p.num_n) {
-                    bad = true;
-                    continue;
-                }
-                const int pos = atomicAdd(&cnt_out[crow + n], 1);
-                if (pos < p.num_m) idx_out[(crow + n) * p.num_m + pos] = m;
-                else bad = true;  // a tile listed twice in one row overflows its column
-            }
+    for (int list = 0; list < 2; ++list) {
+        const int32_t *cnt_in = list ? p.mask_cnt : p.full_cnt;
+        const int32_t *idx_in = list ? p.mask_idx : p.full_idx;
+        int c = cnt_in[w];
+        if (c < 0 || c > p.num_n) {
+            bad = true;
+            c = c < 0 ? 0 : p.num_n;
         }
-        __syncthreads();  // the next (smaller) m is appended after this one
+        const uint32_t code = list ? 2u : 1u;
+        for (int e = lane; e < c; e += 32) {
+            const int n = idx_in[w * p.num_n + e];
+            if (n < 0 || n >= p.num_n) {
+                bad = true;
+                continue;
+            }
+            const uint32_t sh = 2u * (uint32_t)(m & 15);
+            const uint32_t old = atomicOr(p.tbits + (bh * p.num_n + n) * p.tbits_words + (m >> 4), code << sh);
+            if ((old >> sh) & 3u) bad = true;
+        }
     }
-    for (long long e = threadIdx.x; e < (long long)p.num_n * p.num_m; e += blockDim.x) {
-        const long long n = e / p.num_m;
-        const int k = (int)(e - n * p.num_m);
-        if (k >= min(p.t_full_cnt[crow + n], p.num_m)) p.t_full_idx[(crow + n) * p.num_m + k] = -1;
-        if (k >= min(p.t_mask_cnt[crow + n], p.num_m)) p.t_mask_idx[(crow + n) * p.num_m + k] = -1;
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_INDEX);
+}
+
+// One warp per KV tile (b, h, n): its column of codes, read from the last Q tile
+// to the first 32 at a time, compacted by ballot into the full and mask lists.
+__global__ void __launch_bounds__(256) bsattn_bwd_scan_kernel(BwdParams p) {
+    const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31u;
+    if (w >= (long long)p.B * p.H * p.num_n) return;
+    const uint32_t *col = p.tbits + w * p.tbits_words;
+    int32_t *fi = p.t_full_idx + w * p.num_m;
+    int32_t *mi = p.t_mask_idx + w * p.num_m;
+    const uint32_t below = (1u << lane) - 1u;
+    int nf = 0, nm = 0;
+    for (int top = p.num_m - 1; top >= 0; top -= 32) {
+        const int m = top - (int)lane;
+        const uint32_t code = m >= 0 ? (col[m >> 4] >> (2u * (uint32_t)(m & 15))) & 3u : 0u;
+        const uint32_t bf = __ballot_sync(0xffffffffu, code == 1u);
+        const uint32_t bm = __ballot_sync(0xffffffffu, code >= 2u);
+        if (code == 1u) fi[nf + __popc(bf & below)] = m;
+        if (code >= 2u) mi[nm + __popc(bm & below)] = m;
+        nf += __popc(bf);
+        nm += __popc(bm);
+    }
+    if (lane == 0) {
+        p.t_full_cnt[w] = nf;
+        p.t_mask_cnt[w] = nm;
+    }
+}
+
+// One CTA: KV tiles ordered by their number of listed Q tiles, longest first (a
+// counting sort; the order among equal lengths is unspecified and affects only
+// which CTA starts first, never a result).
+constexpr int kOrderBins = 8192;
+__global__ void __launch_bounds__(1024) bsattn_bwd_order_kernel(BwdParams p) {
+    __shared__ int hist[kOrderBins];
+    __shared__ int warp_sums[32];
+    const int items = p.B * p.H * p.num_n;
+    const int top = min(p.num_m, kOrderBins - 1);  // lengths above `top` share bin 0
+    const int nb = top + 1;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < items; i += blockDim.x) {
+        const int len = min(p.t_full_cnt[i] + p.t_mask_cnt[i], top);
+        atomicAdd(&hist[top - len], 1);
     }
     __syncthreads();
-    for (int n = threadIdx.x; n < p.num_n; n += blockDim.x) {
-        p.t_full_cnt[crow + n] = min(p.t_full_cnt[crow + n], p.num_m);
-        p.t_mask_cnt[crow + n] = min(p.t_mask_cnt[crow + n], p.num_m);
+    // exclusive scan over the bins: each thread owns a contiguous run of bins
+    const int per = (nb + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int b0 = min((int)threadIdx.x * per, nb), b1 = min(b0 + per, nb);
+    int run = 0;
+    for (int i = b0; i < b1; ++i) run += hist[i];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = run;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_INDEX);
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int v = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_sums[lane] = v;
+    }
+    __syncthreads();
+    int base = incl - run + (wid > 0 ? warp_sums[wid - 1] : 0);
+    for (int i = b0; i < b1; ++i) {
+        const int c = hist[i];
+        hist[i] = base;
+        base += c;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < items; i += blockDim.x) {
+        const int len = min(p.t_full_cnt[i] + p.t_mask_cnt[i], top);
+        p.order[atomicAdd(&hist[top - len], 1)] = i;
+    }
 }
 
 // ------------------------------------------------------------ 2. row pass --
@@ -120,12 +191,18 @@ struct BwdCfg {
     static constexpr uint32_t kSt = 2 * kTileBytes;           // stage s: kSt + s * 2 * kTileBytes
     static constexpr uint32_t kVec = kSt + 4 * kTileBytes;   // stage s: 2 x 128 floats at kVec + 1024 s
     static constexpr uint32_t kBar = kVec + 2048;
-    static constexpr int bRF = 0, bF = 1, bE = 3, bSR = 5, bPR = 6, bDone = 7, bDrain = 8, kNumBars = 9;
+    // barriers: resident tiles full, stage full [2], stage empty [2], S ready,
+    // elementwise done (first / second half), accumulators done, MMA drain
+    static constexpr int bRF = 0, bF = 1, bE = 3, bSR = 5, bPR = 6, bPR2 = 7, bDone = 8, bDrain = 9;
+    static constexpr int kNumBars = 10;
     static constexpr uint32_t kInfo = kBar + kNumBars * 8;    // int32 [2][4]
     static constexpr uint32_t kMisc = kInfo + 32;             // [0] tmem base, [1] abort
     static constexpr uint32_t kBytes = kMisc + 16;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
+
+constexpr int kBwdThreads = 384;  // warps 0-3: roles; warps 4-11: elementwise
+constexpr int kEwWarps = 8;
 
 __device__ __forceinline__ uint32_t bwd_span_bits(long long lo, long long hi) {
     lo = lo < 0 ? 0 : lo;
@@ -147,7 +224,8 @@ __device__ __forceinline__ void bwd_init(uint8_t *gbase, uint32_t base, uint32_t
             mbar_init(bar(C::bE + s), 1);
         }
         mbar_init(bar(C::bSR), 1);
-        mbar_init(bar(C::bPR), 4);  // one arrival per elementwise warp
+        mbar_init(bar(C::bPR), kEwWarps);  // one arrival per elementwise warp
+        mbar_init(bar(C::bPR2), kEwWarps);
         mbar_init(bar(C::bDone), 1);
         mbar_init(bar(C::bDrain), 1);
         misc[1] = 0;
@@ -186,15 +264,40 @@ __device__ __forceinline__ void bwd_store_row32(void *dst, int f32, long long of
     }
 }
 
-// ----------------------------------------------------------- 3. dK and dV --
-// One CTA per (b, h, KV tile n), 256 threads: warp 0 loads (K and V of the tile
-// once, then Q, dO, LSE2 and D of each listed Q tile into a two-stage ring),
-// warp 1 issues the MMAs, warp 2 owns TMEM, warps 4-7 (one per TMEM lane
-// quarter; thread = key row) form P^T and dS^T and write the gradients.
-// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 256 + D), dK [256 + D, 256 + 2D);
-// P^T (bf16) overwrites the first 64 columns of S^T, dS^T those of dP^T.
+// Epilogue of an elementwise warp: its 32 rows x D/2 columns of an fp32 TMEM
+// accumulator (columns [cg * D/2, (cg + 1) * D/2)), times `mul`, to global rows
+// (zeros when `have` is false; nothing stored when `store` is false).
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__device__ __forceinline__ void bwd_epilogue_half(uint32_t tacc, bool have, bool store, void *dst, int f32,
+                                                  long long orow, int cg, float mul) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        const int col = cg * (D / 2) + 32 * c;
+        uint32_t v[32];
+        if (have) {
+            tmem_ld32(tacc + (uint32_t)col, v);
+            tmem_wait_ld();
+            reg_fence(v);
+        } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = 0u;
+        }
+        if (store) bwd_store_row32(dst, f32, orow + col, v, mul);
+    }
+}
+
+// ----------------------------------------------------------- 4. dK and dV --
+// One CTA per (b, h, KV tile n), taken in the order of the order pass; 384
+// threads: warp 0 loads (K and V of the tile once, then Q, dO, LSE2 and D of
+// each listed Q tile into a two-stage ring), warp 1 issues the MMAs, warp 2 owns
+// TMEM, warps 4-11 form P^T and dS^T (warp w: TMEM lane quarter w % 4, thread =
+// key row; column group (w - 4) / 4 takes query columns [32 cg, 32 cg + 32) of
+// each half) and write the gradients.
+// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 256 + D), dK [256 + D, 256 + 2D).
+// P^T (bf16) of query chunk c (32 columns) goes to columns [32 c, 32 c + 16) of
+// S^T, inside the chunk's own fp32 columns, and dS^T likewise within dP^T.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
                            const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                            const __grid_constant__ CUtensorMap tdo) {
@@ -210,10 +313,10 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t warp = warp_id(), lane = lane_id();
     const uint32_t lead = lane == 0 ? 1u : 0u;
 
-    const int n = (int)(blockIdx.x % (unsigned)p.num_n);
-    const int bh = (int)(blockIdx.x / (unsigned)p.num_n);
+    const long long crow = p.order[blockIdx.x];  // (b, h, n) of this CTA
+    const int n = (int)(crow % p.num_n);
+    const int bh = (int)(crow / p.num_n);
     const int b = bh / p.H, h = bh - b * p.H;
-    const long long crow = (long long)bh * p.num_n + n;
     const int cm = min(max(p.t_mask_cnt[crow], 0), p.num_m);
     const int cf = min(max(p.t_full_cnt[crow], 0), p.num_m);
     const int total = cm + cf;  // listed Q tiles: the mask list, then the full list
@@ -282,18 +385,24 @@ __global__ void __launch_bounds__(256, 1)
                 mma_ss_lead(lead, tP, dVk + off, dOk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
             mma_commit_lead(lead, bar(C::bSR));
-            if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
             const uint64_t dOm = smem_desc_sw128(st + C::kTileBytes, C::kSubBytes, 1024);
             const uint64_t dQm = smem_desc_sw128(st, C::kSubBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)  // dV += P^T dO
-                mma_ts_lead(lead, tdV, tS + kk * 8, dOm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
-                            (it > 0 || kk > 0) ? 1u : 0u);
+            for (int half = 0; half < 2; ++half) {
+                if (!(ok = mbar_wait(bar(half ? C::bPR2 : C::bPR), it & 1, abort_flag, p.err,
+                                     BSATTN_FLAG_TIMEOUT)))
+                    break;
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)  // dK += dS^T Q
-                mma_ts_lead(lead, tdK, tP + kk * 8, dQm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
-                            (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // dV += P^T dO (16 queries per step)
+                    mma_ts_lead(lead, tdV, tS + 32u * (kk >> 1) + 8u * (kk & 1),
+                                dOm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // dK += dS^T Q
+                    mma_ts_lead(lead, tdK, tP + 32u * (kk >> 1) + 8u * (kk & 1),
+                                dQm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!ok) break;
             mma_commit_lead(lead, bar(C::bE + s));  // stage free once these have read it
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
@@ -302,6 +411,7 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------- elementwise --
         const uint32_t q4 = warp & 3u;
+        const int cg = (int)(warp - 4) >> 2;   // column group
         const int r = (int)(q4 * 32u + lane);  // key row of the tile
         const uint32_t la = (q4 * 32u) << 16;  // TMEM lane offset of this warp
         const int j = n * kTile + r;           // sequence-local key
@@ -339,7 +449,8 @@ __global__ void __launch_bounds__(256, 1)
             const int32_t dk = doc ? p.doc_k[(long long)b * p.seqlen_k + j] : 0;
             const float *l2 = vecs + s * 256, *dd = l2 + 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int half = 0; half < 2; ++half) {
+                const int c = 2 * half + cg;  // query chunk: columns [32 c, 32 c + 32)
                 uint32_t vs[32], vp[32];
                 tmem_ld32(tS + la + 32u * c, vs);
                 tmem_ld32(tP + la + 32u * c, vp);
@@ -369,13 +480,13 @@ __global__ void __launch_bounds__(256, 1)
                     pw[x] = pack_bf16x2(p0, p1);
                     dw[x] = pack_bf16x2(ds0, ds1);
                 }
-                tmem_st16(tS + la + 16u * c, pw);
-                tmem_st16(tP + la + 16u * c, dw);
+                tmem_st16(tS + la + 32u * c, pw);
+                tmem_st16(tP + la + 32u * c, dw);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(half ? C::bPR2 : C::bPR));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::bPR));
         }
         // ------------------------------------------------- epilogue --
         if (ok && total > 0) {
@@ -383,28 +494,9 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
         }
         if (ok) {
-            const bool store = j < p.seqlen_k;
             const long long orow = (((long long)b * p.seqlen_k + j) * p.H + h) * D;
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint32_t tacc = g ? tdK : tdV;
-                const float mul = g ? p.scale : 1.f;
-                void *dst = g ? p.dk : p.dv;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (total > 0) {
-                        tmem_ld32(tacc + la + 32u * c, v);
-                        tmem_wait_ld();
-                        reg_fence(v);
-                    } else {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) v[x] = 0u;
-                    }
-                    if (!store) continue;
-                    bwd_store_row32(dst, p.grad_f32, orow + 32 * c, v, mul);
-                }
-            }
+            bwd_epilogue_half<D>(tdV + la, total > 0, j < p.seqlen_k, p.dv, p.grad_f32, orow, cg, 1.f);
+            bwd_epilogue_half<D>(tdK + la, total > 0, j < p.seqlen_k, p.dk, p.grad_f32, orow, cg, p.scale);
         }
     }
     tc_fence_before();
@@ -415,15 +507,18 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-// ------------------------------------------------------------------ 4. dQ --
-// One CTA per (b, h, Q tile m), 256 threads, the same roles: Q and dO of the tile
-// stay resident, K and V of each listed KV tile (the forward's mask list, then
-// its full list; entries outside [0, num_n) skipped by every role alike) pass
-// through the two-stage ring.  Thread = query row.
-// TMEM: S [0, 128), dP [128, 256), dQ [256, 256 + D); dS (bf16) overwrites the
-// first 64 columns of dP.
+// ------------------------------------------------------------------ 5. dQ --
+// One CTA per (b, h, Q tile m), 384 threads, the same roles: Q and dO of the
+// tile stay resident, K and V of each listed KV tile (the forward's mask list,
+// then its full list; entries outside [0, num_n) skipped by every role alike)
+// pass through the two-stage ring.  Thread = query row; column group cg of the
+// elementwise warps takes key chunks 2 cg and 2 cg + 1.
+// TMEM: S [0, 128), dP [128, 256), dS buffers (bf16) [256, 320) and [320, 384),
+// dQ [384, 384 + D).  The MMA warp issues S and dP of tile t + 1 as soon as the
+// elementwise warps have finished tile t, then the dQ product of tile t, which
+// reads dS buffer t % 2 while the elementwise warps fill the other one.
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap tdo) {
@@ -455,7 +550,7 @@ __global__ void __launch_bounds__(256, 1)
 
     bwd_init<D>(gbase, base, warp);
     const uint32_t tmem = misc[0];
-    const uint32_t tS = tmem, tP = tmem + 128u, tdQ = tmem + 256u;
+    const uint32_t tS = tmem, tP = tmem + 128u, tDS = tmem + 256u, tdQ = tmem + 384u;
 
     if (warp == 0) {
         // ------------------------------------------------------- loads --
@@ -495,32 +590,46 @@ __global__ void __launch_bounds__(256, 1)
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dQk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dOk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-        tc_fence_after();
-        for (int it = 0; ok && it < total; ++it) {
-            const int s = it & 1;
-            if (!(ok = mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
+        // S = Q K^T and dP = dO V^T of the tile in stage s, then commit SR
+        auto issue_s_dp = [&](int s) {
             const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
             const uint64_t dKk = smem_desc_sw128(st, 16, 1024);
             const uint64_t dVk = smem_desc_sw128(st + C::kTileBytes, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
                 mma_ss_lead(lead, tS, dQk + off, dKk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
                 mma_ss_lead(lead, tP, dOk + off, dVk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
             mma_commit_lead(lead, bar(C::bSR));
+        };
+        bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+        tc_fence_after();
+        if (ok && total > 0) {
+            ok = mbar_wait(bar(C::bF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+            tc_fence_after();
+            if (ok) issue_s_dp(0);
+        }
+        for (int it = 0; ok && it < total; ++it) {
+            const int s = it & 1;
             if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
+            if (it + 1 < total) {
+                if (!(ok = mbar_wait(bar(C::bF + (s ^ 1)), ((it + 1) >> 1) & 1, abort_flag, p.err,
+                                     BSATTN_FLAG_TIMEOUT)))
+                    break;
+                tc_fence_after();
+                issue_s_dp(s ^ 1);
+            }
+            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
             const uint64_t dKm = smem_desc_sw128(st, C::kSubBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)  // dQ += dS K
-                mma_ts_lead(lead, tdQ, tP + kk * 8, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
+            for (int kk = 0; kk < kTile / 16; ++kk)  // dQ += dS K (16 keys per step)
+                mma_ts_lead(lead, tdQ, tDS + 64u * s + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
                             (it > 0 || kk > 0) ? 1u : 0u);
             mma_commit_lead(lead, bar(C::bE + s));
         }
@@ -530,6 +639,7 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------- elementwise --
         const uint32_t q4 = warp & 3u;
+        const int cg = (int)(warp - 4) >> 2;
         const int r = (int)(q4 * 32u + lane);  // query row of the tile
         const uint32_t la = (q4 * 32u) << 16;
         const int i = m * kTile + r;           // sequence-local query
@@ -565,7 +675,8 @@ __global__ void __launch_bounds__(256, 1)
             }
             const bool doc = msk && p.kind == BSATTN_MASK_DOCUMENT;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int x2 = 0; x2 < 2; ++x2) {
+                const int c = 2 * cg + x2;  // key chunk: columns [32 c, 32 c + 32)
                 uint32_t vs[32], vp[32];
                 tmem_ld32(tS + la + 32u * c, vs);
                 tmem_ld32(tP + la + 32u * c, vp);
@@ -590,7 +701,7 @@ __global__ void __launch_bounds__(256, 1)
                         ((keep >> (2 * x + 1)) & 1u) ? ex2_approx(fmaf(__uint_as_float(vs[2 * x + 1]), sl2, -l2)) : 0.f;
                     dw[x] = pack_bf16x2(p0 * (__uint_as_float(vp[2 * x]) - dd), p1 * (__uint_as_float(vp[2 * x + 1]) - dd));
                 }
-                tmem_st16(tP + la + 16u * c, dw);
+                tmem_st16(tDS + 64u * s + la + 16u * c, dw);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -603,22 +714,8 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
         }
         if (ok) {
-            const bool store = i < p.seqlen_q;
             const long long orow = (((long long)b * p.seqlen_q + i) * p.H + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                if (total > 0) {
-                    tmem_ld32(tdQ + la + 32u * c, v);
-                    tmem_wait_ld();
-                    reg_fence(v);
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) v[x] = 0u;
-                }
-                if (!store) continue;
-                bwd_store_row32(p.dq, p.grad_f32, orow + 32 * c, v, p.scale);
-            }
+            bwd_epilogue_half<D>(tdQ + la, total > 0, i < p.seqlen_q, p.dq, p.grad_f32, orow, cg, p.scale);
         }
     }
     tc_fence_before();
@@ -655,20 +752,27 @@ cudaError_t prepare_bwd_kernels() {
     return cudaSuccess;
 }
 
+unsigned warp_blocks(long long warps) { return (unsigned)((warps + 7) / 8); }
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream) {
     cudaError_t e = prepare_bwd_kernels<D>();
     if (e != cudaSuccess) return e;
     const long long bh = (long long)p.B * p.H;
-    bsattn_bwd_transpose_kernel<<<(unsigned)bh, 256, 0, stream>>>(p);
+    const size_t bits_bytes = (size_t)bh * p.num_n * p.tbits_words * sizeof(uint32_t);
+    if ((e = cudaMemsetAsync(p.tbits, 0, bits_bytes, stream)) != cudaSuccess) return e;
+    bsattn_bwd_scatter_kernel<<<warp_blocks(bh * p.num_m), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long long rows = bh * p.num_m * kTile;
-    bsattn_bwd_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    bsattn_bwd_scan_kernel<<<warp_blocks(bh * p.num_n), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_dkdv_kernel<D><<<(unsigned)(bh * p.num_n), 256, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
+    bsattn_bwd_order_kernel<<<1, 1024, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_dq_kernel<D><<<(unsigned)(bh * p.num_m), 256, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
+    bsattn_bwd_rows_kernel<<<warp_blocks(bh * p.num_m * kTile), 256, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bsattn_bwd_dkdv_kernel<D><<<(unsigned)(bh * p.num_n), kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bsattn_bwd_dq_kernel<D><<<(unsigned)(bh * p.num_m), kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 

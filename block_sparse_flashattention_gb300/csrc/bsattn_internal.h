@@ -90,6 +90,9 @@ struct BwdParams {
     float scale, scale_log2;
     const int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;  // forward lists
     int32_t *t_full_cnt, *t_full_idx, *t_mask_cnt, *t_mask_idx; // KV-major: [B, H, num_n(, num_m)]
+    uint32_t *tbits;              // 2-bit codes [B, H, num_n][tbits_words], 16 Q tiles per word
+    int tbits_words;              // ceil(num_m / 16)
+    int32_t *order;               // [B * H * num_n] KV tiles, longest list first
     const int32_t *vl;            // [B, num_n] or null (mask tiles only)
     int kind, window_left, sink_tokens, prefix_len;
     const int32_t *doc_q, *doc_k;

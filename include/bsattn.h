@@ -383,8 +383,10 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
 
 /*
  * bsattn_bwd_workspace_size -- bytes of workspace bsattn_bwd needs for this
- * (batched) metadata: the KV-major transpose of the lists (4 (2 + 2 num_m)
- * bytes per KV tile and head) plus two fp32 values per padded query row.
+ * (batched) metadata: per KV tile and head, the KV-major transpose of the lists,
+ * a 2-bit selection code per Q tile and a slot of the launch order (4 (3 + 2
+ * num_m) + 4 ceil(num_m / 16) bytes), plus two fp32 values per padded query row;
+ * each of the eight regions rounded up to 256 bytes.
  * Varlen -> BSATTN_ERR_UNSUPPORTED.
  */
 bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes);

@@ -264,13 +264,14 @@ def test_bwd_rejects_bad_arguments(kw, expect):
 
 
 def test_bwd_workspace_size():
-    # counts 2 x [B*H*num_n] int32, lists 2 x [B*H*num_n*num_m] int32, rows 2 x
+    # counts 2 x [B*H*num_n] int32, lists 2 x [B*H*num_n*num_m] int32, 2-bit codes
+    # [B*H*num_n*ceil(num_m/16)] uint32, order [B*H*num_n] int32, rows 2 x
     # [B*H*num_m*128] fp32, each region rounded up to 256 bytes
     up = lambda x: -(-x // 256) * 256  # noqa: E731
-    assert bsa.bsattn_bwd_workspace_size(_meta()) == 2 * 256 + 2 * 256 + 2 * 2048
-    m = _meta(B=3, H=5, num_m=7, num_n=9)
-    assert bsa.bsattn_bwd_workspace_size(m) == (2 * up(4 * 135) + 2 * up(4 * 135 * 7)
-                                                + 2 * up(4 * 105 * 128))
+    assert bsa.bsattn_bwd_workspace_size(_meta()) == 3 * 256 + 2 * 256 + 256 + 2 * 2048
+    m = _meta(B=3, H=5, num_m=17, num_n=9)
+    assert bsa.bsattn_bwd_workspace_size(m) == (3 * up(4 * 135) + 2 * up(4 * 135 * 17)
+                                                + up(4 * 135 * 2) + 2 * up(4 * 255 * 128))
     with pytest.raises(bsa.BsattnError):
         bsa.bsattn_bwd_workspace_size(_meta(varlen=1, cu_total_m_blocks=FAKE,
                                             cu_block_idx_offsets=FAKE))
