@@ -191,10 +191,11 @@ struct BwdCfg {
     static constexpr uint32_t kSt = 2 * kTileBytes;           // stage s: kSt + s * 2 * kTileBytes
     static constexpr uint32_t kVec = kSt + 4 * kTileBytes;   // stage s: 2 x 128 floats at kVec + 1024 s
     static constexpr uint32_t kBar = kVec + 2048;
-    // barriers: resident tiles full, stage full [2], stage empty [2], S ready,
-    // elementwise done (first / second half), accumulators done, MMA drain
-    static constexpr int bRF = 0, bF = 1, bE = 3, bSR = 5, bPR = 6, bPR2 = 7, bDone = 8, bDrain = 9;
-    static constexpr int kNumBars = 10;
+    // barriers: resident tiles full, stage full [2], stage empty [2], S and dP
+    // ready (first / second half of the tile), elementwise done (first / second
+    // half), accumulators done, MMA drain
+    static constexpr int bRF = 0, bF = 1, bE = 3, bSR = 5, bSR2 = 6, bPR = 7, bPR2 = 8, bDone = 9;
+    static constexpr int bDrain = 10, kNumBars = 11;
     static constexpr uint32_t kInfo = kBar + kNumBars * 8;    // int32 [2][4]
     static constexpr uint32_t kMisc = kInfo + 32;             // [0] tmem base, [1] abort
     static constexpr uint32_t kBytes = kMisc + 16;
@@ -224,6 +225,7 @@ __device__ __forceinline__ void bwd_init(uint8_t *gbase, uint32_t base, uint32_t
             mbar_init(bar(C::bE + s), 1);
         }
         mbar_init(bar(C::bSR), 1);
+        mbar_init(bar(C::bSR2), 1);
         mbar_init(bar(C::bPR), kEwWarps);  // one arrival per elementwise warp
         mbar_init(bar(C::bPR2), kEwWarps);
         mbar_init(bar(C::bDone), 1);
@@ -360,50 +362,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMAs --
-        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
+        // Per listed Q tile, in two query halves h (N = 64): S^T_h, dP^T_h -> SR_h;
+        // after PR_h, dV and dK over half h.  Half h of the next tile is issued
+        // right after this tile's half-h gradient products, so the tensor core
+        // works on one half while the elementwise warps work on the other.
+        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dKk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dVk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-        tc_fence_after();
-        for (int it = 0; ok && it < total; ++it) {
-            const int s = it & 1;
-            if (!(ok = mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
+        auto issue_s = [&](int s, int half) {  // S^T = K Q_h^T, dP^T = V dO_h^T (rows 64 h.. of the stage)
+            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u;
             const uint64_t dQk = smem_desc_sw128(st, 16, 1024);
             const uint64_t dOk = smem_desc_sw128(st + C::kTileBytes, 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tS, dKk + off, dQk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, tS + 64u * half, dKk + off, dQk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tP, dVk + off, dOk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, tP + 64u * half, dVk + off, dOk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
-            mma_commit_lead(lead, bar(C::bSR));
+            mma_commit_lead(lead, bar(half ? C::bSR2 : C::bSR));
+        };
+        auto issue_grad = [&](int s, int half, int it) {  // dV += P^T_h dO_h, dK += dS^T_h Q_h
+            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
             const uint64_t dOm = smem_desc_sw128(st + C::kTileBytes, C::kSubBytes, 1024);
             const uint64_t dQm = smem_desc_sw128(st, C::kSubBytes, 1024);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (!(ok = mbar_wait(bar(half ? C::bPR2 : C::bPR), it & 1, abort_flag, p.err,
+            for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // 16 queries per step
+                mma_ts_lead(lead, tdV, tS + 32u * (kk >> 1) + 8u * (kk & 1),
+                            dOm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+                mma_ts_lead(lead, tdK, tP + 32u * (kk >> 1) + 8u * (kk & 1),
+                            dQm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+        tc_fence_after();
+        if (ok && total > 0) {
+            ok = mbar_wait(bar(C::bF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+            tc_fence_after();
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(0, 1);
+            }
+        }
+        for (int it = 0; ok && it < total; ++it) {
+            const int s = it & 1;
+            const bool more = it + 1 < total;
+            if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
+            tc_fence_after();
+            issue_grad(s, 0, it);
+            if (more) {
+                if (!(ok = mbar_wait(bar(C::bF + (s ^ 1)), ((it + 1) >> 1) & 1, abort_flag, p.err,
                                      BSATTN_FLAG_TIMEOUT)))
                     break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // dV += P^T dO (16 queries per step)
-                    mma_ts_lead(lead, tdV, tS + 32u * (kk >> 1) + 8u * (kk & 1),
-                                dOm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // dK += dS^T Q
-                    mma_ts_lead(lead, tdK, tP + 32u * (kk >> 1) + 8u * (kk & 1),
-                                dQm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+                issue_s(s ^ 1, 0);
             }
-            if (!ok) break;
+            if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
+            tc_fence_after();
+            issue_grad(s, 1, it);
             mma_commit_lead(lead, bar(C::bE + s));  // stage free once these have read it
+            if (more) issue_s(s ^ 1, 1);
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
         mma_commit_lead(lead, bar(C::bDrain));
@@ -423,10 +447,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int it = 0; it < total; ++it) {
             const int s = it & 1;
-            bool w = mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            w = w && mbar_wait(bar(C::bSR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            if (!(ok = __all_sync(0xffffffffu, w))) break;
-            tc_fence_after();
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err,
+                                                         BSATTN_FLAG_TIMEOUT))))
+                break;
             const int m = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 0];
             const bool msk = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 1] != 0;
             // kept query columns of this key row: [lo, hi) (query i = m * 128 + column)
@@ -450,6 +473,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float *l2 = vecs + s * 256, *dd = l2 + 128;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(half ? C::bSR2 : C::bSR), it & 1, abort_flag,
+                                                             p.err, BSATTN_FLAG_TIMEOUT))))
+                    break;
+                tc_fence_after();
                 const int c = 2 * half + cg;  // query chunk: columns [32 c, 32 c + 32)
                 uint32_t vs[32], vp[32];
                 tmem_ld32(tS + la + 32u * c, vs);
@@ -487,6 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(half ? C::bPR2 : C::bPR));
             }
+            if (!ok) break;
         }
         // ------------------------------------------------- epilogue --
         if (ok && total > 0) {
@@ -512,11 +540,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // tile stay resident, K and V of each listed KV tile (the forward's mask list,
 // then its full list; entries outside [0, num_n) skipped by every role alike)
 // pass through the two-stage ring.  Thread = query row; column group cg of the
-// elementwise warps takes key chunks 2 cg and 2 cg + 1.
+// elementwise warps takes key chunk 2 h + cg of key half h.
 // TMEM: S [0, 128), dP [128, 256), dS buffers (bf16) [256, 320) and [320, 384),
-// dQ [384, 384 + D).  The MMA warp issues S and dP of tile t + 1 as soon as the
-// elementwise warps have finished tile t, then the dQ product of tile t, which
-// reads dS buffer t % 2 while the elementwise warps fill the other one.
+// dQ [384, 384 + D).  S and dP are formed in two key halves; half h of tile t + 1
+// is issued as soon as the elementwise warps have finished half h of tile t,
+// before that half's dQ product, which reads dS buffer t % 2 while the
+// elementwise warps fill the other one.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
@@ -545,8 +574,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int n = e < cm ? __ldg(p.mask_idx + crow * p.num_n + e) : __ldg(p.full_idx + crow * p.num_n + (e - cm));
         return (n >= 0 && n < p.num_n) ? n : -1;
     };
-    int total = 0;  // valid entries: counted by every thread the same way
-    for (int e = 0; e < cm + cf; ++e) total += entry(e) >= 0 ? 1 : 0;
+    int total = 0;  // valid entries: every warp counts them 32 at a time
+    for (int e0 = 0; e0 < cm + cf; e0 += 32) {
+        const int e = e0 + (int)(threadIdx.x & 31u);
+        total += __popc(__ballot_sync(0xffffffffu, e < cm + cf && entry(e) >= 0));
+    }
 
     bwd_init<D>(gbase, base, warp);
     const uint32_t tmem = misc[0];
@@ -585,52 +617,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMAs --
-        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
+        // Per listed KV tile, in two key halves h (N = 64): S_h, dP_h -> SR_h; after
+        // PR_h, half h of the next tile's S and dP, then dQ += dS_h K_h of this one.
+        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dQk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dOk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        // S = Q K^T and dP = dO V^T of the tile in stage s, then commit SR
-        auto issue_s_dp = [&](int s) {
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
+        auto issue_s = [&](int s, int half) {  // S_h = Q K_h^T, dP_h = dO V_h^T (rows 64 h.. of the stage)
+            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u;
             const uint64_t dKk = smem_desc_sw128(st, 16, 1024);
             const uint64_t dVk = smem_desc_sw128(st + C::kTileBytes, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tS, dQk + off, dKk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, tS + 64u * half, dQk + off, dKk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tP, dOk + off, dVk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, tP + 64u * half, dOk + off, dVk + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
-            mma_commit_lead(lead, bar(C::bSR));
+            mma_commit_lead(lead, bar(half ? C::bSR2 : C::bSR));
+        };
+        auto issue_dq = [&](int s, int half, int it) {  // dQ += dS_h K_h (16 keys per step)
+            const uint64_t dKm = smem_desc_sw128(base + C::kSt + (uint32_t)s * 2u * C::kTileBytes, C::kSubBytes, 1024);
+#pragma unroll
+            for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+                mma_ts_lead(lead, tdQ, tDS + 64u * s + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
+                            (it > 0 || kk > 0) ? 1u : 0u);
         };
         bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
         tc_fence_after();
         if (ok && total > 0) {
             ok = mbar_wait(bar(C::bF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
             tc_fence_after();
-            if (ok) issue_s_dp(0);
+            if (ok) {
+                issue_s(0, 0);
+                issue_s(0, 1);
+            }
         }
         for (int it = 0; ok && it < total; ++it) {
             const int s = it & 1;
+            const bool more = it + 1 < total;
             if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
-            if (it + 1 < total) {
+            if (more) {
                 if (!(ok = mbar_wait(bar(C::bF + (s ^ 1)), ((it + 1) >> 1) & 1, abort_flag, p.err,
                                      BSATTN_FLAG_TIMEOUT)))
                     break;
                 tc_fence_after();
-                issue_s_dp(s ^ 1);
+                issue_s(s ^ 1, 0);
             }
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
-            const uint64_t dKm = smem_desc_sw128(st, C::kSubBytes, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)  // dQ += dS K (16 keys per step)
-                mma_ts_lead(lead, tdQ, tDS + 64u * s + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
-                            (it > 0 || kk > 0) ? 1u : 0u);
+            issue_dq(s, 0, it);
+            if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
+            tc_fence_after();
+            if (more) issue_s(s ^ 1, 1);
+            issue_dq(s, 1, it);
             mma_commit_lead(lead, bar(C::bE + s));
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
@@ -651,10 +694,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int it = 0; it < total; ++it) {
             const int s = it & 1;
-            bool w = mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            w = w && mbar_wait(bar(C::bSR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            if (!(ok = __all_sync(0xffffffffu, w))) break;
-            tc_fence_after();
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err,
+                                                         BSATTN_FLAG_TIMEOUT))))
+                break;
             const int n = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 0];
             const bool msk = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 1] != 0;
             int lim = min(kTile, p.seqlen_k - n * kTile);
@@ -675,8 +717,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             const bool doc = msk && p.kind == BSATTN_MASK_DOCUMENT;
 #pragma unroll
-            for (int x2 = 0; x2 < 2; ++x2) {
-                const int c = 2 * cg + x2;  // key chunk: columns [32 c, 32 c + 32)
+            for (int half = 0; half < 2; ++half) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(half ? C::bSR2 : C::bSR), it & 1, abort_flag,
+                                                             p.err, BSATTN_FLAG_TIMEOUT))))
+                    break;
+                tc_fence_after();
+                const int c = 2 * half + cg;  // key chunk: columns [32 c, 32 c + 32)
                 uint32_t vs[32], vp[32];
                 tmem_ld32(tS + la + 32u * c, vs);
                 tmem_ld32(tP + la + 32u * c, vp);
@@ -702,11 +748,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dw[x] = pack_bf16x2(p0 * (__uint_as_float(vp[2 * x]) - dd), p1 * (__uint_as_float(vp[2 * x + 1]) - dd));
                 }
                 tmem_st16(tDS + 64u * s + la + 16u * c, dw);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(half ? C::bPR2 : C::bPR));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::bPR));
+            if (!ok) break;
         }
         // ------------------------------------------------- epilogue --
         if (ok && total > 0) {
