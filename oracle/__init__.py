@@ -1,4 +1,5 @@
-"""CPU oracle for the block-sparse attention forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the block-sparse attention forward and its backward -- TEST
+INFRASTRUCTURE ONLY.
 
 Loads ``bsattn_oracle.c`` (plain C, fp64; compiled here with gcc) through
 ctypes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -9,7 +10,10 @@ Functions follow the varlen block-sparsity pull request (flash-attention
 #2224, description and review) for the metadata layout and the block-sparse
 learning note ("Dense FlashAttention vs Block-Sparse Attention", section 2) for
 the reversed, -1-padded index lists; the C file's header lists each source and
-every reading taken where the pages leave a step open.
+every reading taken where the pages leave a step open.  The backward (numpy,
+fp64: ``bwd_f64`` and its per-tile forms) differentiates the same definition;
+it is pinned by central finite differences and fp64 torch autograd, and the
+per-tile forms by the dense one (tests/test_oracle_bwd.py).
 """
 from __future__ import annotations
 
@@ -450,3 +454,103 @@ def bwd_f64(wl, meta, qf, kf, vf, gf):
 def bwd(wl, q, k, v, meta, dout):
     """bwd_f64 on bf16 inputs (raw bits); dQ, dK, dV in the layouts of q, k, v."""
     return bwd_f64(wl, meta, _widen(q), _widen(k), _widen(v), _widen(dout))
+
+
+# ---- per-tile backward, for sampled checks at full size.  The same definition
+# as bwd_f64 (gradients of softmax attention over each row's allowed keys),
+# evaluated for one Q tile's rows or one KV tile's keys: a row's probabilities
+# involve only the keys its Q tile's lists name, so nothing outside them is
+# formed, and only the slices used are widened from bf16.
+
+def _pred(wl, b, i, j):
+    """Token predicate of the mask kind for query rows i (column vector) and keys
+    j (row vector) of sequence b, as in allowed_mask."""
+    if wl.kind == 0:
+        return np.ones((i.shape[0], j.shape[1]), bool)
+    if wl.kind == 1:
+        return j <= i
+    if wl.kind == 2:
+        return (j <= i) & ((i - j < wl.window_left) | (j < wl.sink_tokens))
+    if wl.kind == 4:
+        return (j < wl.prefix_len) | (j <= i)
+    if wl.kind == 3:
+        Sq, Sk = int(wl.seqlens_q[b]), int(wl.seqlens_k[b])
+        dq = np.asarray(wl.doc_id_q)[b * Sq:(b + 1) * Sq]
+        dk = np.asarray(wl.doc_id_k)[b * Sk:(b + 1) * Sk]
+        return dq[i[:, 0]][:, None] == dk[j[0]][None, :]
+    raise ValueError(wl.kind)
+
+
+def tile_allowed(wl, meta, b, h, m):
+    """Q tile m of (b, h): (r0, r1, keys, A) with rows [r0, r1), `keys` the
+    ascending key indices of the tiles its lists name, and A bool [rows, keys]
+    the allowed pairs (full tiles: keys below seqlen_k; mask tiles: also the
+    token predicate and the tile's valid length); a tile named twice is one
+    tile whose allowed pairs are the union."""
+    Sq, Sk = int(wl.seqlens_q[b]), int(wl.seqlens_k[b])
+    tm, tn = wl.tile_m, wl.tile_n
+    r0, r1 = m * tm, min((m + 1) * tm, Sq)
+    i = np.arange(r0, r1)[:, None]
+    blocks = {}
+    for key, masked in (("full", False), ("mask", True)):
+        cnt = int(meta[key + "_cnt"][b, h, m])
+        for n in meta[key + "_idx"][b, h, m, :cnt]:
+            n = int(n)
+            c0, c1 = n * tn, min((n + 1) * tn, Sk)
+            if c1 <= c0:
+                continue
+            blk = np.ones((r1 - r0, c1 - c0), bool)
+            if masked:
+                blk &= _pred(wl, b, i, np.arange(c0, c1)[None, :])
+                if wl.kv_valid_len is not None:
+                    blk &= (np.arange(c1 - c0) < int(wl.kv_valid_len[b, n]))[None, :]
+            blocks[n] = blocks[n] | blk if n in blocks else blk
+    if not blocks:
+        return r0, r1, np.zeros(0, np.int64), np.zeros((r1 - r0, 0), bool)
+    ns = sorted(blocks)
+    keys = np.concatenate([np.arange(n * tn, n * tn + blocks[n].shape[1]) for n in ns])
+    return r0, r1, keys, np.concatenate([blocks[n] for n in ns], axis=1)
+
+
+def _tile_grads(wl, q, k, v, dout, meta, b, h, m):
+    """For Q tile m: rows, keys, P, dS (fp64) and the widened q rows / keys."""
+    r0, r1, keys, A = tile_allowed(wl, meta, b, h, m)
+    qf = _widen(q[b, r0:r1, h])
+    kf, vf = _widen(k[b, keys, h]), _widen(v[b, keys, h])
+    g = _widen(dout[b, r0:r1, h])
+    s = np.where(A, wl.scale * (qf @ kf.T), -np.inf)
+    mx = s.max(axis=1, keepdims=True) if keys.size else np.zeros((r1 - r0, 1))
+    mx = np.where(np.isfinite(mx), mx, 0.0)
+    e = np.where(A, np.exp(s - mx), 0.0)
+    den = e.sum(axis=1, keepdims=True)
+    P = np.divide(e, den, out=np.zeros_like(e), where=den > 0)
+    O = P @ vf
+    dS = P * (g @ vf.T - (g * O).sum(axis=1, keepdims=True))
+    return r0, r1, keys, P, dS, qf, kf, g
+
+
+def bwd_dq_tile(wl, q, k, v, dout, meta, b, h, m):
+    """dQ (fp64 [rows, D]) of Q tile m of (b, h); inputs are raw bf16 bits in the
+    batched layout, `meta` the oracle's own lists."""
+    _, _, keys, _, dS, _, kf, _ = _tile_grads(wl, q, k, v, dout, meta, b, h, m)
+    return wl.scale * (dS @ kf) if keys.size else np.zeros((dS.shape[0], q.shape[3]))
+
+
+def bwd_dkdv_tile(wl, q, k, v, dout, meta, b, h, n):
+    """(dK, dV) (fp64 [keys, D] each) of KV tile n of (b, h): the sums over every Q
+    tile whose lists name n."""
+    Sk = int(wl.seqlens_k[b])
+    c0, c1 = n * wl.tile_n, min((n + 1) * wl.tile_n, Sk)
+    D = q.shape[3]
+    dk, dv = np.zeros((c1 - c0, D)), np.zeros((c1 - c0, D))
+    for m in range(meta["full_cnt"].shape[2]):
+        named = any(n in meta[key + "_idx"][b, h, m, :int(meta[key + "_cnt"][b, h, m])]
+                    for key in ("full", "mask"))
+        if not named:
+            continue
+        _, _, keys, P, dS, qf, _, g = _tile_grads(wl, q, k, v, dout, meta, b, h, m)
+        sel = (keys >= c0) & (keys < c1)
+        pos = keys[sel] - c0
+        dv[pos] += P[:, sel].T @ g
+        dk[pos] += wl.scale * (dS[:, sel].T @ qf)
+    return dk, dv

@@ -21,6 +21,7 @@ CASES = [
     dict(seed=203, B=1, H=1, D=8, seqlens_q=[256], seqlens_k=[400], kind=MASK_PREFIX,
          prefix_len=150, valid_len=True),
     dict(seed=204, B=1, H=2, D=8, seqlens_q=[260], kind=MASK_NONE, density=0.6),
+    dict(seed=205, B=2, H=1, D=8, seqlens_q=[300, 300], kind=MASK_DOCUMENT, density=0.8),
 ]
 
 
@@ -74,3 +75,29 @@ def test_dense_causal_matches_torch_autograd():
     o.backward(torch.tensor(G.transpose(0, 2, 1, 3)))
     for ref, got in ((tq.grad, dq), (tk.grad, dk), (tv.grad, dv)):
         assert np.max(np.abs(ref.numpy().transpose(0, 2, 1, 3) - got)) < 1e-10
+
+
+@pytest.mark.parametrize("c", CASES)
+def test_per_tile_backward_equals_the_dense_one(c):
+    # the per-tile forms (for sampled checks at full size) against bwd_f64 on
+    # every Q tile and KV tile, and their allowed sets against allowed_mask
+    wl = random_workload(**c)
+    q, k, v = wl.qkv()
+    g = wl.tensor("do")
+    meta = oracle.build_meta(wl)
+    dq, dk, dv = oracle.bwd(wl, q, k, v, meta, g)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            A = oracle.allowed_mask(wl, meta, b, h)
+            for m in range(wl.num_m):
+                r0, r1, keys, At = oracle.tile_allowed(wl, meta, b, h, m)
+                full = np.zeros((r1 - r0, A.shape[1]), bool)
+                full[:, keys] = At
+                assert np.array_equal(full, A[r0:r1])
+                t = oracle.bwd_dq_tile(wl, q, k, v, g, meta, b, h, m)
+                assert np.max(np.abs(t - dq[b, r0:r1, h]), initial=0) < 1e-12
+            for n in range(wl.num_n):
+                tk, tv = oracle.bwd_dkdv_tile(wl, q, k, v, g, meta, b, h, n)
+                c0 = n * wl.tile_n
+                assert np.max(np.abs(tk - dk[b, c0:c0 + tk.shape[0], h]), initial=0) < 1e-12
+                assert np.max(np.abs(tv - dv[b, c0:c0 + tv.shape[0], h]), initial=0) < 1e-12
