@@ -332,8 +332,6 @@ def time_bwd(wl, dw, meta, out, lse, err, stream, flop_fwd, iters=5):
     convention; the kernels recompute S and dP once more (seven products)."""
     import torch
     import block_sparse_flashattention_gb300 as bsa
-    if wl.varlen:
-        return {"note": "varlen backward not provided (batched only)"}
     dev = dw.q.device
     sq, sk = dw.seqlens()
     hdo = torch.empty(wl.q_shape(), dtype=torch.int16, pin_memory=True)
@@ -346,7 +344,8 @@ def time_bwd(wl, dw, meta, out, lse, err, stream, flop_fwd, iters=5):
 
     def bwd():
         st = bsa.bsattn_bwd(dw.q, dw.k, dw.v, out, bsa.OUT_BF16, lse, dout, wl.B, sq, sk, wl.H,
-                            wl.D, meta, dw.vl, wl.kind, dw.mask_params, wl.scale, dq, dk, dv,
+                            wl.D, dw.cu_q, dw.cu_k, meta, dw.vl, wl.kind, dw.mask_params, wl.scale,
+                            dq, dk, dv,
                             bsa.OUT_BF16, wsb, err_flag=err, stream=stream.cuda_stream)
         if st != bsa.BSATTN_OK:
             raise RuntimeError(bsa.status_string(st))

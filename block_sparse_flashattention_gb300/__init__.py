@@ -129,20 +129,24 @@ def forward(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None, kv_val
     return out, lse
 
 
-def backward(q, k, v, out, lse, dout, meta: Meta, *, kv_valid_len=None, kind: int = MASK_NONE,
-             mask_params: Optional[MaskParams] = None, softmax_scale: Optional[float] = None,
-             grad_dtype=None, workspace=None, err_flag=None, stream=None):
-    """Gradients (dq, dk, dv) of ``forward`` (batched) for upstream gradient dout.
+def backward(q, k, v, out, lse, dout, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None,
+             kv_valid_len=None, kind: int = MASK_NONE, mask_params: Optional[MaskParams] = None,
+             softmax_scale: Optional[float] = None, grad_dtype=None, workspace=None,
+             err_flag=None, stream=None):
+    """Gradients (dq, dk, dv) of ``forward`` for upstream gradient dout.
 
-    q/k/v/dout: bf16 [B, S, H, D]; out, lse: the forward's results for the same
+    q/k/v/dout: bf16 [B, S, H, D] or packed [total, H, D] (varlen, with
+    cu_seqlens_q / cu_seqlens_k); out, lse: the forward's results for the same
     arguments.  Gradients are bf16 by default, or torch.float32.  workspace: a
     uint8 tensor of at least bsattn_bwd_workspace_size(meta) bytes, or None to
     allocate one for this call."""
     import torch
     if meta.varlen:
-        raise BsattnError(BSATTN_ERR_UNSUPPORTED, "backward (varlen)")
-    B, seqlen_q, H, D = q.shape
-    seqlen_k = k.shape[1]
+        rows_q, H, D = q.shape
+        seqlen_q, seqlen_k = rows_q, k.shape[0]
+    else:
+        _, seqlen_q, H, D = q.shape
+        seqlen_k = k.shape[1]
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     if grad_dtype is None:
@@ -156,8 +160,8 @@ def backward(q, k, v, out, lse, dout, meta: Meta, *, kv_valid_len=None, kind: in
         workspace = torch.empty(bsattn_bwd_workspace_size(meta), dtype=torch.uint8, device=q.device)
     gd = OUT_F32 if grad_dtype == torch.float32 else OUT_BF16
     od = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
-    _check(bsattn_bwd(q, k, v, out, od, lse, dout, B, seqlen_q, seqlen_k, H, D, meta, kv_valid_len,
-                      kind, mask_params, softmax_scale, dq, dk, dv, gd, workspace,
-                      err_flag=err_flag, stream=stream),
+    _check(bsattn_bwd(q, k, v, out, od, lse, dout, meta.B, seqlen_q, seqlen_k, H, D, cu_seqlens_q,
+                      cu_seqlens_k, meta, kv_valid_len, kind, mask_params, softmax_scale, dq, dk, dv,
+                      gd, workspace, err_flag=err_flag, stream=stream),
            "bsattn_bwd")
     return dq, dk, dv

@@ -99,7 +99,8 @@ def library() -> ctypes.CDLL:
         lib.bsattn_bwd.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-            ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(bsattn_meta), ctypes.c_void_p,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.POINTER(bsattn_meta), ctypes.c_void_p,
             ctypes.c_int, ctypes.POINTER(bsattn_mask_params), ctypes.c_float, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
             ctypes.c_void_p, ctypes.c_void_p]
@@ -295,7 +296,7 @@ def bsattn_fwd_workspace_size(meta: Meta) -> int:
 
 
 def bsattn_bwd(q, k, v, out, out_dtype: int, lse, dout, B: int, seqlen_q: int, seqlen_k: int,
-               H: int, D: int, meta: Meta, kv_valid_len, kind: int,
+               H: int, D: int, cu_seqlens_q, cu_seqlens_k, meta: Meta, kv_valid_len, kind: int,
                mask_params: Optional[MaskParams], softmax_scale: float, dq, dk, dv,
                grad_dtype: int, workspace, workspace_bytes: int = 0, err_flag=None,
                stream=None) -> int:
@@ -306,14 +307,15 @@ def bsattn_bwd(q, k, v, out, out_dtype: int, lse, dout, B: int, seqlen_q: int, s
         workspace_bytes = workspace.numel() * workspace.element_size()
     return library().bsattn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), int(out_dtype), _ptr(lse), _ptr(dout), int(B),
-        int(seqlen_q), int(seqlen_k), int(H), int(D), ctypes.byref(mt), _ptr(kv_valid_len),
+        int(seqlen_q), int(seqlen_k), int(H), int(D), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        ctypes.byref(mt), _ptr(kv_valid_len),
         int(kind), ctypes.byref(mp) if mp is not None else None, float(softmax_scale), _ptr(dq),
         _ptr(dk), _ptr(dv), int(grad_dtype), _ptr(workspace), int(workspace_bytes),
         _ptr(err_flag), _stream(stream))
 
 
 def bsattn_bwd_workspace_size(meta: Meta) -> int:
-    """Bytes of workspace bsattn_bwd needs for `meta` (batched)."""
+    """Bytes of workspace bsattn_bwd needs for `meta`."""
     mt = meta.to_c()
     n = ctypes.c_size_t(0)
     st = library().bsattn_bwd_workspace_size(ctypes.byref(mt), ctypes.byref(n))

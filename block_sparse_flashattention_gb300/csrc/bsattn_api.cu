@@ -267,31 +267,32 @@ bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, i
 }
 
 // Workspace of bsattn_bwd, in 256-byte aligned regions: the KV-major counts
-// (full, mask) [B, H, num_n], the KV-major lists (full, mask) [B, H, num_n,
-// num_m], the 2-bit selection matrix [B, H, num_n][ceil(num_m / 16)] uint32, the
-// KV tile order [B * H * num_n], then LSE * log2(e) and D, fp32 [B * H][num_m *
-// 128] each.
+// (full, mask) and the KV tile order, [B, H, num_n] int32 each (varlen: [H,
+// B num_n]); the KV-major lists (full, mask), int32, and the selection codes,
+// one byte each, all in the layout of the forward's index lists ([B, H, num_n,
+// num_m] batched, [H, total_n] varlen); the KV tile prefix [B + 1]; then
+// LSE * log2(e) and D, fp32, 128 per Q tile ([B, H, num_m] or [H, total_m]).
 struct BwdLayout {
-    size_t t_full_cnt, t_mask_cnt, t_full_idx, t_mask_idx, tbits, order, lse2, dvec, total;
+    size_t t_full_cnt, t_mask_cnt, order, t_full_idx, t_mask_idx, codes, cu_tn, lse2, dvec, total;
 };
 
 BwdLayout bwd_layout(const bsattn_meta *m) {
     auto up = [](size_t x) { return (x + 255u) & ~(size_t)255u; };
-    const size_t bh = (size_t)m->B * (size_t)m->H;
-    const size_t cnt = up(bh * (size_t)m->num_n * 4u);
-    const size_t idx = up(bh * (size_t)m->num_n * (size_t)m->num_m * 4u);
-    const size_t bits = up(bh * (size_t)m->num_n * (size_t)((m->num_m + 15) / 16) * 4u);
-    const size_t row = up(bh * (size_t)m->num_m * (size_t)kTile * 4u);
+    const size_t cols = (size_t)m->B * (size_t)m->H * (size_t)m->num_n;
+    const size_t entries = m->varlen ? (size_t)m->H * (size_t)m->total_n_blocks : cols * (size_t)m->num_m;
+    const size_t q_tiles = m->varlen ? (size_t)m->H * (size_t)m->total_m_blocks
+                                     : (size_t)m->B * (size_t)m->H * (size_t)m->num_m;
     BwdLayout L;
     L.t_full_cnt = 0;
-    L.t_mask_cnt = L.t_full_cnt + cnt;
-    L.t_full_idx = L.t_mask_cnt + cnt;
-    L.t_mask_idx = L.t_full_idx + idx;
-    L.tbits = L.t_mask_idx + idx;
-    L.order = L.tbits + bits;
-    L.lse2 = L.order + cnt;
-    L.dvec = L.lse2 + row;
-    L.total = L.dvec + row;
+    L.t_mask_cnt = L.t_full_cnt + up(cols * 4u);
+    L.order = L.t_mask_cnt + up(cols * 4u);
+    L.t_full_idx = L.order + up(cols * 4u);
+    L.t_mask_idx = L.t_full_idx + up(entries * 4u);
+    L.codes = L.t_mask_idx + up(entries * 4u);
+    L.cu_tn = L.codes + up(entries);
+    L.lse2 = L.cu_tn + up(((size_t)m->B + 1u) * 4u);
+    L.dvec = L.lse2 + up(q_tiles * (size_t)kTile * 4u);
+    L.total = L.dvec + up(q_tiles * (size_t)kTile * 4u);
     return L;
 }
 
@@ -448,7 +449,7 @@ bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes) 
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
     if (!bytes) return BSATTN_ERR_INVALID_ARG;
-    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;
+    if (meta->varlen && meta->num_n <= 0) return BSATTN_ERR_INVALID_ARG;
     *bytes = bwd_layout(meta).total;
     return BSATTN_OK;
 }
@@ -456,13 +457,13 @@ bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes) 
 bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void *out,
                          bsattn_out_dtype out_dtype, const float *lse, const void *dout, int32_t B,
                          int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                          const bsattn_meta *meta, const int32_t *kv_valid_len, bsattn_mask_kind kind,
                          const bsattn_mask_params *mp, float softmax_scale, void *dq, void *dk, void *dv,
                          bsattn_out_dtype grad_dtype, void *workspace, size_t workspace_bytes,
                          int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
-    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched only
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
         return BSATTN_ERR_INVALID_ARG;
@@ -471,13 +472,23 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
         return BSATTN_ERR_INVALID_ARG;
     if (B <= 0 || H <= 0 || seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
     if (meta->B != B || meta->H != H) return BSATTN_ERR_INVALID_ARG;
-    if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
-        return BSATTN_ERR_INVALID_ARG;
+    long long rows_q, rows_k;
+    if (meta->varlen) {
+        // seqlen_q / seqlen_k: total packed rows, as for bsattn_fwd
+        if (!cu_seqlens_q || !cu_seqlens_k || meta->num_n <= 0) return BSATTN_ERR_INVALID_ARG;
+        rows_q = seqlen_q;
+        rows_k = seqlen_k;
+    } else {
+        if (cu_seqlens_q || cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
+        if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+            return BSATTN_ERR_INVALID_ARG;
+        rows_q = (long long)B * seqlen_q;
+        rows_k = (long long)B * seqlen_k;
+    }
     if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BSATTN_ERR_INVALID_ARG;
     if (out_dtype != BSATTN_OUT_BF16 && out_dtype != BSATTN_OUT_F32) return BSATTN_ERR_INVALID_ARG;
     if (grad_dtype != BSATTN_OUT_BF16 && grad_dtype != BSATTN_OUT_F32) return BSATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
-    const long long rows_q = (long long)B * seqlen_q, rows_k = (long long)B * seqlen_k;
     if (rows_q > INT32_MAX || rows_k > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
     const BwdLayout L = bwd_layout(meta);
     if (workspace_bytes < L.total) return BSATTN_ERR_INVALID_ARG;
@@ -494,13 +505,24 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
 
     char *ws = static_cast<char *>(workspace);
     bsattn::BwdParams p = {};
+    p.varlen = meta->varlen ? 1 : 0;
     p.B = B;
     p.H = H;
     p.D = D;
     p.seqlen_q = seqlen_q;
     p.seqlen_k = seqlen_k;
-    p.num_m = meta->num_m;
+    p.num_m = meta->varlen ? 0 : meta->num_m;
     p.num_n = meta->num_n;
+    p.rows_q = rows_q;
+    p.rows_k = rows_k;
+    p.total_m = meta->total_m_blocks;
+    p.total_n = meta->total_n_blocks;
+    p.num_m_max = meta->varlen ? meta->total_m_blocks : meta->num_m;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.cu_tm = meta->cu_total_m_blocks;
+    p.cu_off = meta->cu_block_idx_offsets;
+    p.cu_tn = reinterpret_cast<int32_t *>(ws + L.cu_tn);
     p.scale = softmax_scale;
     p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634074);
     p.full_cnt = meta->full_cnt;
@@ -511,8 +533,7 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
     p.t_mask_cnt = reinterpret_cast<int32_t *>(ws + L.t_mask_cnt);
     p.t_full_idx = reinterpret_cast<int32_t *>(ws + L.t_full_idx);
     p.t_mask_idx = reinterpret_cast<int32_t *>(ws + L.t_mask_idx);
-    p.tbits = reinterpret_cast<uint32_t *>(ws + L.tbits);
-    p.tbits_words = (int)((meta->num_m + 15) / 16);
+    p.codes = reinterpret_cast<uint8_t *>(ws + L.codes);
     p.order = reinterpret_cast<int32_t *>(ws + L.order);
     p.vl = kv_valid_len;
     p.kind = (int)kind;

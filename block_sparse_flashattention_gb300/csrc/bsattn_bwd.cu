@@ -1,30 +1,37 @@
-// Backward of the block-sparse attention forward (batched).  With P the
+// Backward of the block-sparse attention forward, batched or varlen.  With P the
 // forward's probabilities over each row's allowed keys, O = P V and upstream
 // gradient dO:
 //   D_i = sum_d dO_i O_i,  dV = P^T dO,  dP = dO V^T,  dS = P (dP - D),
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // Training needs the backward, which the pages list as missing ("[CuTe,Flex]
-// varlen blocksparsity", flash-attention #2224; "[feat] VSA-256 fastpath",
-// FastVideo #1354).  It runs as
-//   1. list transpose: the forward's (Q tile -> KV tiles) lists are scattered
-//      into a 2-bit matrix per KV tile (none / full / mask for every Q tile),
-//      then one warp per KV tile compacts its column into KV-major lists, Q
-//      tiles in descending order;
+// varlen blocksparsity", flash-attention #2224, which also names the transposed
+// metadata it needs; "[feat] VSA-256 fastpath", FastVideo #1354).  It runs as
+//   0. (varlen) a prefix of the sequences' KV tile counts;
+//   1. list transpose: every forward list entry sets a byte code (1 full, 2
+//      mask) for its (KV tile, Q tile) pair, stored in the layout of the
+//      KV-major lists; one warp per KV tile then compacts its codes into
+//      KV-major full / mask lists, Q tiles in descending order;
 //   2. an order pass: KV tiles sorted by list length, longest first, so the
 //      dK / dV grid starts its longest CTAs first;
-//   3. a row pass writing D and LSE * log2(e) into padded per-(b, h) rows;
+//   3. a row pass writing D and LSE * log2(e) into rows padded to 128 per Q tile;
 //   4. the dK / dV kernel: one CTA per KV tile, S^T = K Q^T and dP^T = V dO^T per
-//      listed Q tile on tcgen05, P^T and dS^T formed per key row in TMEM, then
-//      dV += P^T dO and dK += dS^T Q accumulated in TMEM, handed over in two
-//      halves of the Q tile so that the products of one half overlap the
-//      elementwise work of the other;
+//      listed Q tile on tcgen05 in two query halves, P^T and dS^T formed per key
+//      row in TMEM, dV += P^T dO and dK += dS^T Q accumulated in TMEM; half h of
+//      the next Q tile is issued as soon as this one's half h is done, so the
+//      products of one half overlap the elementwise work of the other;
 //   5. the dQ kernel: one CTA per Q tile, S = Q K^T and dP = dO V^T per listed KV
-//      tile, dS per query row into one of two TMEM buffers, dQ += dS K
-//      accumulated in TMEM; the next tile's S and dP are issued before this
-//      tile's dQ product, so the elementwise work overlaps it.
+//      tile in two key halves, dS per query row into one of two TMEM buffers,
+//      dQ += dS K accumulated in TMEM, pipelined the same way.
 // P is recomputed from the forward's LSE (no running maximum) and rounded to
 // bf16 before the P^T dO product, as the forward rounds it before P V; dS is
 // rounded to bf16 before its products.
+// Layouts.  Batched: sequence b of length S at rows b S; forward lists
+// [B, H, num_m(, num_n)]; KV-major lists [B, H, num_n(, num_m)].  Varlen:
+// sequence b at rows cu_q[b] / cu_k[b]; forward lists [H, total_m] /
+// [H, total_n]; KV-major counts [H, B num_n] (tile cu_tn[b] + n of head h, the
+// rest unused), KV-major lists [H, total_n] with column (b, n) at
+// cu_block_idx_offsets[b] + n num_m(b) (the block of sequence b holds num_m(b)
+// num_n(b) entries in either order).
 #include <cuda_bf16.h>
 
 #include "bsattn_internal.h"
@@ -34,56 +41,221 @@ namespace bsattn {
 
 namespace {
 
+// Geometry of sequence b.  A varlen sequence whose offsets disagree with the
+// metadata (num_m(b) != ceil(len_q / 128), num_n(b) above the kv_valid_len
+// stride, or its list block past total_n) has no tiles here.
+struct Seq {
+    int sq, sk, nm, nn;  // lengths, Q tiles, KV tiles
+    long long q0, k0;    // first packed row
+    int T0, Tk0;         // first packed Q tile, first KV tile (varlen: cu_tn[b])
+    long long off;       // varlen: first entry of the sequence's list block
+    int bad;             // varlen offsets rejected (then nm = nn = 0)
+};
+
+__device__ __forceinline__ Seq seq_of(const BwdParams &p, int b) {
+    Seq s;
+    if (!p.varlen) {
+        s.sq = p.seqlen_q;
+        s.sk = p.seqlen_k;
+        s.nm = p.num_m;
+        s.nn = p.num_n;
+        s.q0 = (long long)b * p.seqlen_q;
+        s.k0 = (long long)b * p.seqlen_k;
+        s.T0 = b * p.num_m;
+        s.Tk0 = b * p.num_n;
+        s.off = 0;
+        s.bad = 0;
+        return s;
+    }
+    s.q0 = p.cu_q[b];
+    s.k0 = p.cu_k[b];
+    s.sq = p.cu_q[b + 1] - p.cu_q[b];
+    s.sk = p.cu_k[b + 1] - p.cu_k[b];
+    s.nm = p.cu_tm[b + 1] - p.cu_tm[b];
+    s.nn = s.sk > 0 ? (s.sk + kTile - 1) / kTile : 0;
+    s.T0 = p.cu_tm[b];
+    s.Tk0 = p.cu_tn ? p.cu_tn[b] : 0;
+    s.off = p.cu_off[b];
+    const bool ok = s.sq >= 0 && s.sk >= 0 && s.nm == (s.sq + kTile - 1) / kTile && s.nn <= p.num_n &&
+                    s.off >= 0 && s.off + (long long)s.nm * s.nn <= p.total_n;
+    s.bad = ok ? 0 : 1;
+    if (!ok) s.nm = s.nn = 0;
+    return s;
+}
+
+// Largest b in [0, B) with cu[b] <= x (cu ascending).
+__device__ __forceinline__ int seq_search(const int32_t *cu, int B, long long x) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Forward list row of (b, h, m): count index and first index entry.
+__device__ __forceinline__ long long fwd_cnt_at(const BwdParams &p, const Seq &s, int b, int h, int m) {
+    return p.varlen ? (long long)h * p.total_m + s.T0 + m : ((long long)b * p.H + h) * p.num_m + m;
+}
+__device__ __forceinline__ long long fwd_idx_at(const BwdParams &p, const Seq &s, int b, int h, int m) {
+    return p.varlen ? (long long)h * p.total_n + s.off + (long long)m * s.nn
+                    : (((long long)b * p.H + h) * p.num_m + m) * p.num_n;
+}
+// KV-major column of (b, h, n): count index (also the order pass's item id) and
+// first list entry (also the first selection code).
+__device__ __forceinline__ long long kv_cnt_at(const BwdParams &p, const Seq &s, int b, int h, int n) {
+    return p.varlen ? (long long)h * p.B * p.num_n + s.Tk0 + n : ((long long)b * p.H + h) * p.num_n + n;
+}
+__device__ __forceinline__ long long kv_idx_at(const BwdParams &p, const Seq &s, int b, int h, int n) {
+    return p.varlen ? (long long)h * p.total_n + s.off + (long long)n * s.nm
+                    : (((long long)b * p.H + h) * p.num_n + n) * p.num_m;
+}
+// First of the 128 padded rows of Q tile (b, h, m) in the LSE2 / D workspace.
+__device__ __forceinline__ long long vec_at(const BwdParams &p, const Seq &s, int b, int h, int m) {
+    return (p.varlen ? (long long)h * p.total_m + s.T0 + m : ((long long)b * p.H + h) * p.num_m + m) * kTile;
+}
+
+// Decodes a KV-major item id into (b, h, n); false for ids past the last tile.
+__device__ __forceinline__ bool kv_item(const BwdParams &p, long long c, int &b, int &h, int &n, Seq &s) {
+    if (!p.varlen) {
+        n = (int)(c % p.num_n);
+        const long long bh = c / p.num_n;
+        b = (int)(bh / p.H);
+        h = (int)(bh - (long long)b * p.H);
+        if (b >= p.B) return false;
+        s = seq_of(p, b);
+        return true;
+    }
+    const long long per_head = (long long)p.B * p.num_n;
+    h = (int)(c / per_head);
+    const long long Tk = c - (long long)h * per_head;
+    if (h >= p.H || Tk >= p.cu_tn[p.B]) return false;
+    b = seq_search(p.cu_tn, p.B, Tk);
+    s = seq_of(p, b);
+    n = (int)(Tk - s.Tk0);
+    return n < s.nn;
+}
+
+// Decodes a packed Q tile id (batched: (b H + h) num_m + m; varlen: h total_m + T)
+// into (b, h, m); false when the tile holds no rows.
+__device__ __forceinline__ bool q_item(const BwdParams &p, long long t, int &b, int &h, int &m, Seq &s) {
+    if (!p.varlen) {
+        m = (int)(t % p.num_m);
+        const long long bh = t / p.num_m;
+        b = (int)(bh / p.H);
+        h = (int)(bh - (long long)b * p.H);
+        if (b >= p.B) return false;
+        s = seq_of(p, b);
+        return true;
+    }
+    h = (int)(t / p.total_m);
+    const int T = (int)(t - (long long)h * p.total_m);
+    if (h >= p.H || T >= p.cu_tm[p.B]) return false;
+    b = seq_search(p.cu_tm, p.B, T);
+    s = seq_of(p, b);
+    m = T - s.T0;
+    return m < s.nm;
+}
+
+// ------------------------------------------------ 0. KV tile prefix (varlen) --
+// One CTA: cu_tn[b] = sum of num_n over the sequences before b (0 for a
+// sequence seq_of rejects, which is flagged BSATTN_FLAG_BAD_SEQLENS).
+__global__ void __launch_bounds__(1024) bsattn_bwd_seq_kernel(BwdParams p) {
+    __shared__ int warp_sums[32];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    bool bad = false;
+    for (int b0 = 0; b0 < p.B; b0 += blockDim.x) {
+        const int b = b0 + (int)threadIdx.x;
+        int v = 0;
+        if (b < p.B) {
+            const Seq s = seq_of(p, b);  // (its Tk0, read before this pass wrote it, is unused)
+            bad |= s.bad != 0;
+            v = s.nn;
+        }
+        int incl = v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        if (lane == 31) warp_sums[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += u;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int before = carry + (wid > 0 ? warp_sums[wid - 1] : 0) + incl - v;
+        if (b < p.B) p.cu_tn[b] = before;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = before + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) p.cu_tn[p.B] = carry;
+    if (__syncthreads_or(bad) && threadIdx.x == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_SEQLENS);
+}
+
 // ------------------------------------------------------- 1. list transpose --
 // One warp per forward list row (b, h, m): every valid entry n sets code 1
-// (full) or 2 (mask) for Q tile m in the 2-bit column of KV tile n.  A count
-// outside [0, num_n], an index outside [0, num_n) or a tile listed twice sets
+// (full) or 2 (mask) for (KV tile n, Q tile m).  A count outside [0, num_n(b)],
+// an index outside [0, num_n(b)) or a tile listed twice sets
 // BSATTN_FLAG_BAD_INDEX; the bad entry is skipped (a repeat keeps the OR of the
 // codes, so a tile in both lists is treated as a mask tile).
 __global__ void __launch_bounds__(256) bsattn_bwd_scatter_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (w >= (long long)p.B * p.H * p.num_m) return;
-    const long long bh = w / p.num_m;
-    const int m = (int)(w - bh * p.num_m);
+    int b, h, m;
+    Seq s;
+    if (!q_item(p, w, b, h, m, s)) return;
+    const long long ca = fwd_cnt_at(p, s, b, h, m), ia = fwd_idx_at(p, s, b, h, m);
     bool bad = false;
     for (int list = 0; list < 2; ++list) {
-        const int32_t *cnt_in = list ? p.mask_cnt : p.full_cnt;
-        const int32_t *idx_in = list ? p.mask_idx : p.full_idx;
-        int c = cnt_in[w];
-        if (c < 0 || c > p.num_n) {
+        int c = (list ? p.mask_cnt : p.full_cnt)[ca];
+        const int32_t *idx_in = (list ? p.mask_idx : p.full_idx) + ia;
+        if (c < 0 || c > s.nn) {
             bad = true;
-            c = c < 0 ? 0 : p.num_n;
+            c = c < 0 ? 0 : s.nn;
         }
         const uint32_t code = list ? 2u : 1u;
         for (int e = lane; e < c; e += 32) {
-            const int n = idx_in[w * p.num_n + e];
-            if (n < 0 || n >= p.num_n) {
+            const int n = idx_in[e];
+            if (n < 0 || n >= s.nn) {
                 bad = true;
                 continue;
             }
-            const uint32_t sh = 2u * (uint32_t)(m & 15);
-            const uint32_t old = atomicOr(p.tbits + (bh * p.num_n + n) * p.tbits_words + (m >> 4), code << sh);
-            if ((old >> sh) & 3u) bad = true;
+            const long long at = kv_idx_at(p, s, b, h, n) + m;  // byte of (n, m)
+            const uint32_t sh = 8u * (uint32_t)(at & 3);
+            const uint32_t old = atomicOr(reinterpret_cast<uint32_t *>(p.codes + (at & ~3ll)), code << sh);
+            if ((old >> sh) & 0xffu) bad = true;
         }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_INDEX);
 }
 
-// One warp per KV tile (b, h, n): its column of codes, read from the last Q tile
-// to the first 32 at a time, compacted by ballot into the full and mask lists.
+// One warp per KV tile (b, h, n): its codes, read from the last Q tile to the
+// first 32 at a time, compacted by ballot into the full and mask lists.
 __global__ void __launch_bounds__(256) bsattn_bwd_scan_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const uint32_t lane = threadIdx.x & 31u;
-    if (w >= (long long)p.B * p.H * p.num_n) return;
-    const uint32_t *col = p.tbits + w * p.tbits_words;
-    int32_t *fi = p.t_full_idx + w * p.num_m;
-    int32_t *mi = p.t_mask_idx + w * p.num_m;
+    int b, h, n;
+    Seq s;
+    if (!kv_item(p, w, b, h, n, s)) return;
+    const long long at = kv_idx_at(p, s, b, h, n);
+    const uint8_t *col = p.codes + at;
+    int32_t *fi = p.t_full_idx + at;
+    int32_t *mi = p.t_mask_idx + at;
     const uint32_t below = (1u << lane) - 1u;
     int nf = 0, nm = 0;
-    for (int top = p.num_m - 1; top >= 0; top -= 32) {
+    for (int top = s.nm - 1; top >= 0; top -= 32) {
         const int m = top - (int)lane;
-        const uint32_t code = m >= 0 ? (col[m >> 4] >> (2u * (uint32_t)(m & 15))) & 3u : 0u;
+        const uint32_t code = m >= 0 ? col[m] : 0u;
         const uint32_t bf = __ballot_sync(0xffffffffu, code == 1u);
         const uint32_t bm = __ballot_sync(0xffffffffu, code >= 2u);
         if (code == 1u) fi[nf + __popc(bf & below)] = m;
@@ -92,27 +264,33 @@ __global__ void __launch_bounds__(256) bsattn_bwd_scan_kernel(BwdParams p) {
         nm += __popc(bm);
     }
     if (lane == 0) {
-        p.t_full_cnt[w] = nf;
-        p.t_mask_cnt[w] = nm;
+        const long long ci = kv_cnt_at(p, s, b, h, n);
+        p.t_full_cnt[ci] = nf;
+        p.t_mask_cnt[ci] = nm;
     }
 }
 
-// One CTA: KV tiles ordered by their number of listed Q tiles, longest first (a
-// counting sort; the order among equal lengths is unspecified and affects only
-// which CTA starts first, never a result).
+// One CTA: the ids of the KV tiles ordered by their number of listed Q tiles,
+// longest first (a counting sort; the order among equal lengths is unspecified
+// and affects only which CTA starts first, never a result).  Ids of no tile
+// (varlen padding of the count array) sort last and are written as -1.
 constexpr int kOrderBins = 8192;
 __global__ void __launch_bounds__(1024) bsattn_bwd_order_kernel(BwdParams p) {
     __shared__ int hist[kOrderBins];
     __shared__ int warp_sums[32];
-    const int items = p.B * p.H * p.num_n;
-    const int top = min(p.num_m, kOrderBins - 1);  // lengths above `top` share bin 0
-    const int nb = top + 1;
+    const long long items = (long long)p.B * p.H * p.num_n;
+    const int top = min(p.num_m_max, kOrderBins - 2);  // lengths above `top` share bin 0
+    const int nb = top + 2;                            // bin top + 1: not a tile
+    auto bin_of = [&](long long c) -> int {
+        int b, h, n;
+        Seq s;
+        if (!kv_item(p, c, b, h, n, s)) return top + 1;
+        const long long ci = kv_cnt_at(p, s, b, h, n);
+        return top - min(p.t_full_cnt[ci] + p.t_mask_cnt[ci], top);
+    };
     for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < items; i += blockDim.x) {
-        const int len = min(p.t_full_cnt[i] + p.t_mask_cnt[i], top);
-        atomicAdd(&hist[top - len], 1);
-    }
+    for (long long c = threadIdx.x; c < items; c += blockDim.x) atomicAdd(&hist[bin_of(c)], 1);
     __syncthreads();
     // exclusive scan over the bins: each thread owns a contiguous run of bins
     const int per = (nb + (int)blockDim.x - 1) / (int)blockDim.x;
@@ -143,27 +321,26 @@ __global__ void __launch_bounds__(1024) bsattn_bwd_order_kernel(BwdParams p) {
         base += c;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < items; i += blockDim.x) {
-        const int len = min(p.t_full_cnt[i] + p.t_mask_cnt[i], top);
-        p.order[atomicAdd(&hist[top - len], 1)] = i;
+    for (long long c = threadIdx.x; c < items; c += blockDim.x) {
+        const int bin = bin_of(c);
+        p.order[atomicAdd(&hist[bin], 1)] = bin == top + 1 ? -1 : (int32_t)c;
     }
 }
 
 // ------------------------------------------------------------ 2. row pass --
-// One warp per query row (b, i, h): D = sum_d dO O in fp32 and LSE * log2(e), in
-// rows of num_m * 128 per (b, h).  Rows past seqlen_q, and rows with no keys
-// (LSE = -inf), get LSE2 = +inf, so every probability they would form is 0.
+// One warp per padded query row (Q tile, r): D = sum_d dO O in fp32 and
+// LSE * log2(e).  Rows past the sequence, and rows with no keys (LSE = -inf),
+// get LSE2 = +inf, so every probability they would form is 0.
 __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const long long per_bh = (long long)p.num_m * kTile;
-    if (w >= (long long)p.B * p.H * per_bh) return;
-    const long long bh = w / per_bh;
-    const int i = (int)(w - bh * per_bh);
-    const int b = (int)(bh / p.H), h = (int)(bh - (long long)b * p.H);
+    int b, h, m;
+    Seq s;
+    if (!q_item(p, w / kTile, b, h, m, s)) return;
+    const int i = m * kTile + (int)(w % kTile);
     float d = 0.f, l2 = INFINITY;
-    if (i < p.seqlen_q) {
-        const long long row = ((long long)b * p.seqlen_q + i) * p.H + h;  // [B, S, H] row
+    if (i < s.sq) {
+        const long long row = (s.q0 + i) * p.H + h;  // packed [rows, H] row
         for (int c = lane; c < p.D; c += 32) {
             const float g = __uint_as_float((uint32_t)p.dout[row * p.D + c] << 16);
             const float o = p.o_f32 ? static_cast<const float *>(p.o)[row * p.D + c]
@@ -171,17 +348,17 @@ __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
             d = fmaf(g, o, d);
         }
         for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        const float lse = p.lse[bh * p.seqlen_q + i];
+        const long long li = p.varlen ? (long long)h * p.rows_q + s.q0 + i : ((long long)b * p.H + h) * s.sq + i;
+        const float lse = p.lse[li];
         l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
     }
     if (lane == 0) {
-        p.dvec[bh * per_bh + i] = d;
-        p.lse2[bh * per_bh + i] = l2;
+        const long long at = vec_at(p, s, b, h, m) + (w % kTile);
+        p.dvec[at] = d;
+        p.lse2[at] = l2;
     }
 }
 
-// Shared memory of both gradient kernels: two resident tiles, a ring of two
-// stages of two tiles plus two 128-float vectors, barriers, item info, misc.
 template <int D>
 struct BwdCfg {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
@@ -288,6 +465,7 @@ __device__ __forceinline__ void bwd_epilogue_half(uint32_t tacc, bool have, bool
     }
 }
 
+
 // ----------------------------------------------------------- 4. dK and dV --
 // One CTA per (b, h, KV tile n), taken in the order of the order pass; 384
 // threads: warp 0 loads (K and V of the tile once, then Q, dO, LSE2 and D of
@@ -315,12 +493,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t warp = warp_id(), lane = lane_id();
     const uint32_t lead = lane == 0 ? 1u : 0u;
 
-    const long long crow = p.order[blockIdx.x];  // (b, h, n) of this CTA
-    const int n = (int)(crow % p.num_n);
-    const int bh = (int)(crow / p.num_n);
-    const int b = bh / p.H, h = bh - b * p.H;
-    const int cm = min(max(p.t_mask_cnt[crow], 0), p.num_m);
-    const int cf = min(max(p.t_full_cnt[crow], 0), p.num_m);
+    const long long item = p.order[blockIdx.x];  // (b, h, n) of this CTA; -1: none
+    int b, h, n;
+    Seq sg;
+    if (item < 0 || !kv_item(p, item, b, h, n, sg)) return;
+    const long long ci = kv_cnt_at(p, sg, b, h, n), li = kv_idx_at(p, sg, b, h, n);
+    const int cm = min(max(p.t_mask_cnt[ci], 0), sg.nm);
+    const int cf = min(max(p.t_full_cnt[ci], 0), sg.nm);
     const int total = cm + cf;  // listed Q tiles: the mask list, then the full list
 
     bwd_init<D>(gbase, base, warp);
@@ -329,7 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- loads --
-        const int kvrow = b * p.seqlen_k + n * kTile;
+        const int kvrow = (int)(sg.k0 + n * kTile);
         mbar_arrive_expect_tx_lead(lead, bar(C::bRF), 2 * C::kTileBytes);
         for (int x = 0; x < C::kSub; ++x) {
             tma_load_3d_lead(lead, base + C::kRes0 + x * C::kSubBytes, &tk, bar(C::bRF), x * 64, h, kvrow);
@@ -339,10 +518,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (; it < total; ++it) {
             const int s = it & 1;
             if (!mbar_wait(bar(C::bE + s), ((it >> 1) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
-            const int m = it < cm ? p.t_mask_idx[crow * p.num_m + it] : p.t_full_idx[crow * p.num_m + (it - cm)];
+            const int m = it < cm ? p.t_mask_idx[li + it] : p.t_full_idx[li + (it - cm)];
             info[s * 4 + 0] = m;
             info[s * 4 + 1] = it < cm ? 1 : 0;
-            const int qrow = b * p.seqlen_q + m * kTile;
+            const int qrow = (int)(sg.q0 + m * kTile);
             const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
             mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), 2 * C::kTileBytes + 1024u);
             for (int x = 0; x < C::kSub; ++x) {
@@ -350,7 +529,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d_lead(lead, st + C::kTileBytes + x * C::kSubBytes, &tdo, bar(C::bF + s), x * 64,
                                  h, qrow);
             }
-            const long long vrow = (long long)bh * p.num_m * kTile + (long long)m * kTile;
+            const long long vrow = vec_at(p, sg, b, h, m);
             bulk_g2s_lead(lead, base + C::kVec + 1024u * s, p.lse2 + vrow, 512u, bar(C::bF + s));
             bulk_g2s_lead(lead, base + C::kVec + 1024u * s + 512u, p.dvec + vrow, 512u, bar(C::bF + s));
         }
@@ -439,7 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = (int)(q4 * 32u + lane);  // key row of the tile
         const uint32_t la = (q4 * 32u) << 16;  // TMEM lane offset of this warp
         const int j = n * kTile + r;           // sequence-local key
-        const int klim_full = min(kTile, p.seqlen_k - n * kTile);
+        const int klim_full = min(kTile, sg.sk - n * kTile);
         int klim_mask = klim_full;
         if (p.vl) klim_mask = min(klim_mask, p.vl[(long long)b * p.num_n + n]);
         const float sl2 = p.scale_log2;
@@ -469,7 +648,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
             const bool doc = msk && row_on && p.kind == BSATTN_MASK_DOCUMENT;
-            const int32_t dk = doc ? p.doc_k[(long long)b * p.seqlen_k + j] : 0;
+            const int32_t dk = doc ? p.doc_k[sg.k0 + j] : 0;
             const float *l2 = vecs + s * 256, *dd = l2 + 128;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -489,7 +668,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     keep = 0u;
                     for (int x = 0; x < 32; ++x) {
                         const int i = m * kTile + 32 * c + x;
-                        if (i < p.seqlen_q && __ldg(p.doc_q + (long long)b * p.seqlen_q + i) == dk)
+                        if (i < sg.sq && __ldg(p.doc_q + sg.q0 + i) == dk)
                             keep |= 1u << x;
                     }
                 }
@@ -522,9 +701,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
         }
         if (ok) {
-            const long long orow = (((long long)b * p.seqlen_k + j) * p.H + h) * D;
-            bwd_epilogue_half<D>(tdV + la, total > 0, j < p.seqlen_k, p.dv, p.grad_f32, orow, cg, 1.f);
-            bwd_epilogue_half<D>(tdK + la, total > 0, j < p.seqlen_k, p.dk, p.grad_f32, orow, cg, p.scale);
+            const long long orow = ((sg.k0 + j) * p.H + h) * D;
+            bwd_epilogue_half<D>(tdV + la, total > 0, j < sg.sk, p.dv, p.grad_f32, orow, cg, 1.f);
+            bwd_epilogue_half<D>(tdK + la, total > 0, j < sg.sk, p.dk, p.grad_f32, orow, cg, p.scale);
         }
     }
     tc_fence_before();
@@ -563,16 +742,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t warp = warp_id(), lane = lane_id();
     const uint32_t lead = lane == 0 ? 1u : 0u;
 
-    const int m = (int)(blockIdx.x % (unsigned)p.num_m);
-    const int bh = (int)(blockIdx.x / (unsigned)p.num_m);
-    const int b = bh / p.H, h = bh - b * p.H;
-    const long long crow = (long long)bh * p.num_m + m;
-    const int cm = min(max(p.mask_cnt[crow], 0), p.num_n);
-    const int cf = min(max(p.full_cnt[crow], 0), p.num_n);
+    int b, h, m;
+    Seq sg;
+    if (!q_item(p, blockIdx.x, b, h, m, sg)) return;
+    const long long ca = fwd_cnt_at(p, sg, b, h, m), ia = fwd_idx_at(p, sg, b, h, m);
+    const int cm = min(max(p.mask_cnt[ca], 0), sg.nn);
+    const int cf = min(max(p.full_cnt[ca], 0), sg.nn);
     // raw entry e of the item sequence (mask list first); -1 when out of range
     auto entry = [&](int e) -> int {
-        const int n = e < cm ? __ldg(p.mask_idx + crow * p.num_n + e) : __ldg(p.full_idx + crow * p.num_n + (e - cm));
-        return (n >= 0 && n < p.num_n) ? n : -1;
+        const int n = e < cm ? __ldg(p.mask_idx + ia + e) : __ldg(p.full_idx + ia + (e - cm));
+        return (n >= 0 && n < sg.nn) ? n : -1;
     };
     int total = 0;  // valid entries: every warp counts them 32 at a time
     for (int e0 = 0; e0 < cm + cf; e0 += 32) {
@@ -586,7 +765,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- loads --
-        const int qrow = b * p.seqlen_q + m * kTile;
+        const int qrow = (int)(sg.q0 + m * kTile);
         mbar_arrive_expect_tx_lead(lead, bar(C::bRF), 2 * C::kTileBytes);
         for (int x = 0; x < C::kSub; ++x) {
             tma_load_3d_lead(lead, base + C::kRes0 + x * C::kSubBytes, &tq, bar(C::bRF), x * 64, h, qrow);
@@ -600,7 +779,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!mbar_wait(bar(C::bE + s), ((it >> 1) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
             info[s * 4 + 0] = n;
             info[s * 4 + 1] = e < cm ? 1 : 0;
-            const int kvrow = b * p.seqlen_k + n * kTile;
+            const int kvrow = (int)(sg.k0 + n * kTile);
             const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
             mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), 2 * C::kTileBytes);
             for (int x = 0; x < C::kSub; ++x) {
@@ -686,11 +865,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = (int)(q4 * 32u + lane);  // query row of the tile
         const uint32_t la = (q4 * 32u) << 16;
         const int i = m * kTile + r;           // sequence-local query
-        const long long vrow = (long long)bh * p.num_m * kTile + (long long)m * kTile + r;
+        const long long vrow = vec_at(p, sg, b, h, m) + r;
         const float l2 = p.lse2[vrow], dd = p.dvec[vrow];
         const float sl2 = p.scale_log2;
-        const int32_t dqid = (p.kind == BSATTN_MASK_DOCUMENT && i < p.seqlen_q)
-                                 ? p.doc_q[(long long)b * p.seqlen_q + i] : 0;
+        const int32_t dqid = (p.kind == BSATTN_MASK_DOCUMENT && i < sg.sq) ? p.doc_q[sg.q0 + i] : 0;
         bool ok = true;
         for (int it = 0; it < total; ++it) {
             const int s = it & 1;
@@ -699,7 +877,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             const int n = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 0];
             const bool msk = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 1] != 0;
-            int lim = min(kTile, p.seqlen_k - n * kTile);
+            int lim = min(kTile, sg.sk - n * kTile);
             if (msk && p.vl) lim = min(lim, __ldg(p.vl + (long long)b * p.num_n + n));
             // kept key columns: span [lo0, hi0) plus span [lo1, hi1), cut to [0, lim)
             const long long d = (long long)i - (long long)n * kTile;  // column of key j == i
@@ -735,7 +913,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const uint32_t in_lim = bwd_span_bits(0, (long long)lim - 32 * c);
                     for (int x = 0; x < 32; ++x) {
                         const int j = n * kTile + 32 * c + x;
-                        if (((in_lim >> x) & 1u) && __ldg(p.doc_k + (long long)b * p.seqlen_k + j) == dqid)
+                        if (((in_lim >> x) & 1u) && __ldg(p.doc_k + sg.k0 + j) == dqid)
                             keep |= 1u << x;
                     }
                 }
@@ -761,8 +939,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
         }
         if (ok) {
-            const long long orow = (((long long)b * p.seqlen_q + i) * p.H + h) * D;
-            bwd_epilogue_half<D>(tdQ + la, total > 0, i < p.seqlen_q, p.dq, p.grad_f32, orow, cg, p.scale);
+            const long long orow = ((sg.q0 + i) * p.H + h) * D;
+            bwd_epilogue_half<D>(tdQ + la, total > 0, i < sg.sq, p.dq, p.grad_f32, orow, cg, p.scale);
         }
     }
     tc_fence_before();
@@ -806,20 +984,31 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
                          const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream) {
     cudaError_t e = prepare_bwd_kernels<D>();
     if (e != cudaSuccess) return e;
-    const long long bh = (long long)p.B * p.H;
-    const size_t bits_bytes = (size_t)bh * p.num_n * p.tbits_words * sizeof(uint32_t);
-    if ((e = cudaMemsetAsync(p.tbits, 0, bits_bytes, stream)) != cudaSuccess) return e;
-    bsattn_bwd_scatter_kernel<<<warp_blocks(bh * p.num_m), 256, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_scan_kernel<<<warp_blocks(bh * p.num_n), 256, 0, stream>>>(p);
+    const long long q_tiles = p.varlen ? (long long)p.H * p.total_m : (long long)p.B * p.H * p.num_m;
+    const long long kv_items = (long long)p.B * p.H * p.num_n;
+    const size_t code_bytes = p.varlen ? (size_t)p.H * p.total_n : (size_t)kv_items * p.num_m;
+    if ((e = cudaMemsetAsync(p.codes, 0, (code_bytes + 3) & ~(size_t)3, stream)) != cudaSuccess) return e;
+    if (p.varlen) {
+        bsattn_bwd_seq_kernel<<<1, 1024, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (q_tiles > 0) {
+        bsattn_bwd_scatter_kernel<<<warp_blocks(q_tiles), 256, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    bsattn_bwd_scan_kernel<<<warp_blocks(kv_items), 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bsattn_bwd_order_kernel<<<1, 1024, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_rows_kernel<<<warp_blocks(bh * p.num_m * kTile), 256, 0, stream>>>(p);
+    if (q_tiles > 0) {
+        bsattn_bwd_rows_kernel<<<warp_blocks(q_tiles * kTile), 256, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // every KV tile writes its dK / dV rows (zeros without listed Q tiles)
+    bsattn_bwd_dkdv_kernel<D><<<(unsigned)kv_items, kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_dkdv_kernel<D><<<(unsigned)(bh * p.num_n), kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bsattn_bwd_dq_kernel<D><<<(unsigned)(bh * p.num_m), kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
+    if (q_tiles > 0)
+        bsattn_bwd_dq_kernel<D><<<(unsigned)q_tiles, kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 
@@ -827,10 +1016,10 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
 
 cudaError_t launch_bwd(const BwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tdo, cudaStream_t stream) {
-    const long long bh = (long long)p.B * p.H;
-    if (bh <= 0 || p.num_m <= 0 || p.num_n <= 0) return cudaSuccess;
-    if (bh * p.num_n > 0x7fffffffLL || bh * p.num_m > 0x7fffffffLL ||
-        (bh * p.num_m * kTile + 7) / 8 > 0x7fffffffLL)
+    const long long q_tiles = p.varlen ? (long long)p.H * p.total_m : (long long)p.B * p.H * p.num_m;
+    const long long kv_items = (long long)p.B * p.H * p.num_n;
+    if (kv_items <= 0) return cudaSuccess;
+    if (kv_items > 0x7fffffffLL || q_tiles > 0x7fffffffLL || (q_tiles * kTile + 7) / 8 > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     if (p.D == 64) return launch_bwd_d<64>(p, tq, tk, tv, tdo, stream);
     if (p.D == 128) return launch_bwd_d<128>(p, tq, tk, tv, tdo, stream);

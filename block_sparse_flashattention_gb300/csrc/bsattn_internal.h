@@ -86,21 +86,26 @@ constexpr int kMaxScheduledUnits = 98304;
 // Backward (batched): dK/dV per KV tile over the KV-major lists, dQ per Q tile
 // over the forward lists.
 struct BwdParams {
-    int B, H, D, seqlen_q, seqlen_k, num_m, num_n;
+    int varlen;
+    int B, H, D, seqlen_q, seqlen_k, num_m, num_n;  // varlen: num_m unused, num_n = vl stride
+    long long rows_q, rows_k;     // packed rows (batched: B * seqlen)
+    int total_m, total_n;         // varlen metadata totals
+    int num_m_max;                // longest possible KV-major list (batched num_m, varlen total_m)
+    const int32_t *cu_q, *cu_k, *cu_tm, *cu_off;  // varlen offsets (cu_seqlens, metadata)
+    int32_t *cu_tn;               // varlen workspace [B + 1]: KV tile prefix
     float scale, scale_log2;
     const int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;  // forward lists
-    int32_t *t_full_cnt, *t_full_idx, *t_mask_cnt, *t_mask_idx; // KV-major: [B, H, num_n(, num_m)]
-    uint32_t *tbits;              // 2-bit codes [B, H, num_n][tbits_words], 16 Q tiles per word
-    int tbits_words;              // ceil(num_m / 16)
-    int32_t *order;               // [B * H * num_n] KV tiles, longest list first
+    int32_t *t_full_cnt, *t_full_idx, *t_mask_cnt, *t_mask_idx; // KV-major lists
+    uint8_t *codes;               // selection code per (KV tile, Q tile), list layout
+    int32_t *order;               // [B * H * num_n] KV tile ids, longest list first, -1 padding
     const int32_t *vl;            // [B, num_n] or null (mask tiles only)
     int kind, window_left, sink_tokens, prefix_len;
     const int32_t *doc_q, *doc_k;
-    const void *o;                // forward output, bf16 or fp32 ([B, S_q, H, D])
+    const void *o;                // forward output, bf16 or fp32, layout of q
     int o_f32;
-    const uint16_t *dout;         // bf16 [B, S_q, H, D]
-    const float *lse;             // [B, H, S_q], natural log
-    float *lse2, *dvec;           // workspace [B * H][num_m * 128]: LSE * log2(e), D
+    const uint16_t *dout;         // bf16, layout of q
+    const float *lse;             // batched [B, H, S_q], varlen [H, rows_q]; natural log
+    float *lse2, *dvec;           // workspace, 128 rows per Q tile: LSE * log2(e), D
     void *dq, *dk, *dv;           // gradients in q / k / v layouts
     int grad_f32;
     int32_t *err;

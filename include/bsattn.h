@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define BSATTN_ABI_VERSION 1
+#define BSATTN_ABI_VERSION 2
 
 typedef enum {
     BSATTN_OK = 0,
@@ -345,37 +345,45 @@ bsattn_status bsattn_fwd_static_scratch(const void *q, const void *k, const void
                                         float *lse, int32_t *err_flag, void *stream);
 
 /*
- * bsattn_bwd -- gradients of bsattn_fwd (batched) with respect to q, k and v.
- * The backward is the step the pages report as missing for training ("[CuTe,Flex]
- * varlen blocksparsity", flash-attention #2224: backward not yet supported with
- * block sparsity; "[feat] VSA-256 fastpath", FastVideo #1354: forward only).
+ * bsattn_bwd -- gradients of bsattn_fwd with respect to q, k and v, for batched
+ * and varlen metadata.  The backward is the step the pages report as missing
+ * for training ("[CuTe,Flex] varlen blocksparsity", flash-attention #2224:
+ * backward not yet supported with block sparsity and would need transposed
+ * metadata; "[feat] VSA-256 fastpath", FastVideo #1354: forward only).
  * With P_ij the forward's probabilities (0 outside row i's allowed set A_i, the
  * set bsattn_fwd sums over) and dO the upstream gradient of out:
  *   D_i = sum_d dO_id out_id,   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i),
  *   dv_j = sum_i P_ij dO_i,  dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i.
  * P is recomputed as exp(scale q_i.k_j - lse_i) from the forward's lse; a row
  * with an empty key set (lse = -inf) contributes nothing.  Products run on the
- * tensor cores in bf16 (P and dS rounded to bf16) with fp32 accumulation.
+ * tensor cores in bf16 (P and dS rounded to bf16) with fp32 accumulation; the
+ * result does not depend on the order in which the KV tiles are processed.
  *
- * q, k, v       device bf16 [B, seqlen_*, H, D], 16-byte aligned: the forward's inputs.
- * out, lse      the forward's results for these inputs and this metadata: out
- *               [B, seqlen_q, H, D] in out_dtype, lse fp32 [B, H, seqlen_q].
- * dout          device bf16 [B, seqlen_q, H, D], 16-byte aligned.
- * meta, kv_valid_len, kind, mp, softmax_scale: exactly those given to bsattn_fwd.
+ * q, k, v, B, seqlen_q, seqlen_k, H, D, cu_seqlens_q, cu_seqlens_k, meta,
+ *               kv_valid_len, kind, mp, softmax_scale: exactly those given to
+ *               bsattn_fwd (layouts, varlen packing and checks as there).
+ * out, lse      the forward's results for these arguments: out in the layout of
+ *               q in out_dtype; lse fp32 batched [B, H, seqlen_q], varlen
+ *               [H, total q rows].
+ * dout          device bf16, layout of q, 16-byte aligned.
  * dq, dk, dv    device outputs in the layouts of q, k, v, grad_dtype (fp32 or
- *               bf16), 16-byte aligned; every element is written (rows whose
- *               key or query set is empty get 0).
+ *               bf16), 16-byte aligned; every row of a sequence the metadata
+ *               describes is written (rows whose key or query set is empty get 0).
  * workspace     device, 256-byte aligned, at least bsattn_bwd_workspace_size
  *               bytes; overwritten; needs no zeroing.
  * err_flag      optional device int32 word: BSATTN_FLAG_BAD_INDEX when a list
- *               entry lies outside [0, num_n) (skipped) or a row lists a tile
- *               twice; BSATTN_FLAG_TIMEOUT as for bsattn_fwd.
- * Varlen metadata, D other than 64 or 128 -> BSATTN_ERR_UNSUPPORTED.
+ *               entry lies outside [0, num_n(b)) (skipped), a count outside
+ *               [0, num_n(b)] (clamped) or a row lists a tile twice;
+ *               BSATTN_FLAG_BAD_SEQLENS when a varlen sequence's offsets disagree
+ *               with the metadata (its rows are not written);
+ *               BSATTN_FLAG_TIMEOUT as for bsattn_fwd.
+ * D other than 64 or 128 -> BSATTN_ERR_UNSUPPORTED.
  * Asynchronous on `stream`; the arrays must stay valid until it completes.
  */
 bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void *out,
                          bsattn_out_dtype out_dtype, const float *lse, const void *dout, int32_t B,
                          int32_t seqlen_q, int32_t seqlen_k, int32_t H, int32_t D,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                          const bsattn_meta *meta, const int32_t *kv_valid_len, bsattn_mask_kind kind,
                          const bsattn_mask_params *mp, float softmax_scale, void *dq, void *dk, void *dv,
                          bsattn_out_dtype grad_dtype, void *workspace, size_t workspace_bytes,
@@ -383,11 +391,11 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
 
 /*
  * bsattn_bwd_workspace_size -- bytes of workspace bsattn_bwd needs for this
- * (batched) metadata: per KV tile and head, the KV-major transpose of the lists,
- * a 2-bit selection code per Q tile and a slot of the launch order (4 (3 + 2
- * num_m) + 4 ceil(num_m / 16) bytes), plus two fp32 values per padded query row;
- * each of the eight regions rounded up to 256 bytes.
- * Varlen -> BSATTN_ERR_UNSUPPORTED.
+ * metadata: per KV tile and head (B * num_n per head; varlen: num_n is the
+ * kv_valid_len stride) two list counts and an order slot (12 bytes); per entry
+ * of the forward's index lists two KV-major list entries and a selection code
+ * (9 bytes); B + 1 prefix entries; two fp32 values per Q tile row (1 KB per Q
+ * tile and head); each of the nine regions rounded up to 256 bytes.
  */
 bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
 

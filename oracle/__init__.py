@@ -451,9 +451,47 @@ def bwd_f64(wl, meta, qf, kf, vf, gf):
     return dq, dk, dv
 
 
+def seq_view(wl, meta, b):
+    """Sequence b of a varlen workload as a batched workload of one sequence with
+    its own slice of the lists (varlen layout, flash-attention #2224: counts
+    [H, total_m_blocks] from cu_total_m_blocks[b], indices [H, total_n_blocks]
+    with row (b, m) at cu_block_idx_offsets[b] + m num_n(b)).  Returns (view,
+    meta of the view, packed q-row slice, packed k-row slice)."""
+    from dataclasses import replace
+    sq, sk = int(wl.seqlens_q[b]), int(wl.seqlens_k[b])
+    nm, nn = -(-sq // wl.tile_m), -(-sk // wl.tile_n)
+    t0 = int(meta["cu_total_m_blocks"][b])
+    off = int(meta["cu_block_idx_offsets"][b])
+    mb = {}
+    for key in ("full", "mask"):
+        mb[key + "_cnt"] = np.asarray(meta[key + "_cnt"])[:, t0:t0 + nm][None]
+        mb[key + "_idx"] = np.asarray(meta[key + "_idx"])[:, off:off + nm * nn].reshape(wl.H, nm, nn)[None]
+    cq, ck = wl.cu_seqlens_q, wl.cu_seqlens_k
+    qs, ks = slice(int(cq[b]), int(cq[b + 1])), slice(int(ck[b]), int(ck[b + 1]))
+    view = replace(wl, B=1, varlen=False, seqlens_q=np.array([sq], np.int32),
+                   seqlens_k=np.array([sk], np.int32),
+                   block_map=np.zeros((1, wl.H, nm, nn), np.uint8),
+                   kv_valid_len=None if wl.kv_valid_len is None else np.asarray(wl.kv_valid_len)[b:b + 1],
+                   doc_id_q=None if wl.doc_id_q is None else np.asarray(wl.doc_id_q)[qs],
+                   doc_id_k=None if wl.doc_id_k is None else np.asarray(wl.doc_id_k)[ks])
+    return view, mb, qs, ks
+
+
 def bwd(wl, q, k, v, meta, dout):
-    """bwd_f64 on bf16 inputs (raw bits); dQ, dK, dV in the layouts of q, k, v."""
-    return bwd_f64(wl, meta, _widen(q), _widen(k), _widen(v), _widen(dout))
+    """bwd_f64 on bf16 inputs (raw bits); dQ, dK, dV in the layouts of q, k, v.
+    Varlen: every sequence on its own (no key of one sequence is in another's
+    allowed sets), through seq_view."""
+    if not wl.varlen:
+        return bwd_f64(wl, meta, _widen(q), _widen(k), _widen(v), _widen(dout))
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(wl.B):
+        view, mb, qs, ks = seq_view(wl, meta, b)
+        if qs.stop == qs.start or ks.stop == ks.start:
+            continue
+        g = bwd_f64(view, mb, _widen(q[qs])[None], _widen(k[ks])[None], _widen(v[ks])[None],
+                    _widen(dout[qs])[None])
+        dq[qs], dk[ks], dv[ks] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv
 
 
 # ---- per-tile backward, for sampled checks at full size.  The same definition

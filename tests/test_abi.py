@@ -233,7 +233,8 @@ def test_kv_summaries_rejects_bad_arguments(kw):
 
 def _bwd(**kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, out_dtype=bsa.OUT_F32, lse=FAKE, dout=FAKE, B=1,
-             seqlen_q=256, seqlen_k=256, H=2, D=128, meta=_meta(), kv_valid_len=None,
+             seqlen_q=256, seqlen_k=256, H=2, D=128, cu_seqlens_q=None, cu_seqlens_k=None,
+             meta=_meta(), kv_valid_len=None,
              kind=bsa.MASK_CAUSAL, mask_params=None, softmax_scale=0.125, dq=FAKE, dk=FAKE,
              dv=FAKE, grad_dtype=bsa.OUT_F32, workspace=FAKE, workspace_bytes=1 << 20,
              err_flag=None, stream=0)
@@ -243,7 +244,8 @@ def _bwd(**kw):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(D=96), UNS),
-    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), UNS),
+    (dict(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)), INV),  # no cu_seqlens
+    (dict(cu_seqlens_q=FAKE, cu_seqlens_k=FAKE), INV),            # batched meta with cu_seqlens
     (dict(dout=None), INV),
     (dict(lse=None), INV),
     (dict(dq=FAKE + 2), INV),                                  # not 16-byte aligned
@@ -264,14 +266,20 @@ def test_bwd_rejects_bad_arguments(kw, expect):
 
 
 def test_bwd_workspace_size():
-    # counts 2 x [B*H*num_n] int32, lists 2 x [B*H*num_n*num_m] int32, 2-bit codes
-    # [B*H*num_n*ceil(num_m/16)] uint32, order [B*H*num_n] int32, rows 2 x
-    # [B*H*num_m*128] fp32, each region rounded up to 256 bytes
+    # counts 2 x and order 1 x [B*H*num_n] int32; KV-major lists 2 x int32 and codes
+    # 1 x byte per forward index entry ([B*H*num_m*num_n] batched, [H*total_n]
+    # varlen); prefix [B+1] int32; rows 2 x 128 fp32 per Q tile and head; each
+    # region rounded up to 256 bytes
     up = lambda x: -(-x // 256) * 256  # noqa: E731
-    assert bsa.bsattn_bwd_workspace_size(_meta()) == 3 * 256 + 2 * 256 + 256 + 2 * 2048
+    assert bsa.bsattn_bwd_workspace_size(_meta()) == 3 * 256 + 2 * 256 + 256 + 256 + 2 * 2048
     m = _meta(B=3, H=5, num_m=17, num_n=9)
     assert bsa.bsattn_bwd_workspace_size(m) == (3 * up(4 * 135) + 2 * up(4 * 135 * 17)
-                                                + up(4 * 135 * 2) + 2 * up(4 * 255 * 128))
+                                                + up(135 * 17) + up(4 * 4)
+                                                + 2 * up(4 * 255 * 128))
+    v = _meta(varlen=1, B=4, H=3, num_m=0, num_n=6, total_m_blocks=11, total_n_blocks=40,
+              cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE)
+    assert bsa.bsattn_bwd_workspace_size(v) == (3 * up(4 * 72) + 2 * up(4 * 120) + up(120)
+                                                + up(4 * 5) + 2 * up(4 * 33 * 128))
     with pytest.raises(bsa.BsattnError):
-        bsa.bsattn_bwd_workspace_size(_meta(varlen=1, cu_total_m_blocks=FAKE,
+        bsa.bsattn_bwd_workspace_size(_meta(varlen=1, num_n=0, cu_total_m_blocks=FAKE,
                                             cu_block_idx_offsets=FAKE))

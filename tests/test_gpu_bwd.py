@@ -58,8 +58,9 @@ def _run(c, out_dtype=torch.float32, grad_dtype=torch.float32):
     out, lse = dw.forward(meta, err_flag=err, out_dtype=out_dtype)
     dout_bits = wl.tensor("do")
     dout = bf16_to_device(dout_bits, "cuda")
-    dq, dk, dv = bsa.backward(dw.q, dw.k, dw.v, out, lse, dout, meta, kv_valid_len=dw.vl,
-                              kind=wl.kind, mask_params=dw.mask_params, softmax_scale=wl.scale,
+    dq, dk, dv = bsa.backward(dw.q, dw.k, dw.v, out, lse, dout, meta, cu_seqlens_q=dw.cu_q,
+                              cu_seqlens_k=dw.cu_k, kv_valid_len=dw.vl, kind=wl.kind,
+                              mask_params=dw.mask_params, softmax_scale=wl.scale,
                               grad_dtype=grad_dtype, err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
@@ -73,6 +74,32 @@ def _f64(t):
 @pytest.mark.parametrize("idx", range(len(CASES)))
 def test_backward_matches_oracle(idx):
     wl, dout_bits, grads = _run(CASES[idx])
+    q, k, v = wl.qkv()
+    ref = oracle.bwd(wl, q, k, v, oracle.build_meta(wl), dout_bits)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = _f64(g)
+        scale = max(np.max(np.abs(r)), 1e-30)
+        assert np.max(np.abs(g - r)) <= MAX_TOL * scale, name
+        assert np.linalg.norm(g - r) <= FRO_TOL * max(np.linalg.norm(r), 1e-30), name
+
+
+VARLEN_CASES = [
+    dict(seed=321, B=3, H=2, D=128, seqlens_q=[300, 129, 700], seqlens_k=[260, 400, 900],
+         varlen=True, kind=MASK_CAUSAL, density=0.6),
+    dict(seed=322, B=4, H=2, D=64, seqlens_q=[250, 90, 610, 128], varlen=True,
+         kind=MASK_SLIDING_WINDOW, window_left=200, sink_tokens=30, valid_len=True, density=0.8),
+    dict(seed=323, B=2, H=3, D=128, seqlens_q=[480, 333], varlen=True, kind=MASK_DOCUMENT,
+         density=0.7),
+    dict(seed=324, B=3, H=1, D=64, seqlens_q=[200, 330, 140], seqlens_k=[310, 150, 520],
+         varlen=True, kind=MASK_PREFIX, prefix_len=140, valid_len=True, density=0.7),
+    dict(seed=325, B=2, H=2, D=128, seqlens_q=[640, 384], varlen=True, kind=MASK_NONE,
+         density=0.5, force_diag=False),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(VARLEN_CASES)))
+def test_varlen_backward_matches_oracle(idx):
+    wl, dout_bits, grads = _run(VARLEN_CASES[idx])
     q, k, v = wl.qkv()
     ref = oracle.bwd(wl, q, k, v, oracle.build_meta(wl), dout_bits)
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):

@@ -2,9 +2,10 @@
 bench.py times (bf16 forward output, bf16 gradients), against the oracle.
 
 The batched random workload (B 2, H 4, S 1024) is compared element by element
-with the dense fp64 backward; the VSA (H 24, S 61440) and long-context (H 32,
-S 131072) workloads on sampled Q tiles (dQ rows) and KV tiles (dK, dV rows),
-each computed by the oracle's per-tile backward.  Tolerance as in
+with the dense fp64 backward; the varlen workload (8 sequences of 100-4096
+tokens, H 16), the VSA (H 24, S 61440) and the long-context (H 32, S 131072)
+workloads on sampled Q tiles (dQ rows) and KV tiles (dK, dV rows), each
+computed by the oracle's per-tile backward (per sequence for varlen).  Tolerance as in
 test_gpu_bwd.py, per sampled tensor: max |G - G_ref| <= 2e-2 max |G_ref| and
 ||G - G_ref||_F <= 1e-2 ||G_ref||_F."""
 import numpy as np
@@ -30,8 +31,9 @@ def _run(wl):
     meta = dw.build_meta(err_flag=err)
     out, lse = dw.forward(meta, err_flag=err)
     grads = bsa.backward(dw.q, dw.k, dw.v, out, lse, bf16_to_device(g, "cuda"), meta,
-                         kv_valid_len=dw.vl, kind=wl.kind, mask_params=dw.mask_params,
-                         softmax_scale=wl.scale, err_flag=err)
+                         cu_seqlens_q=dw.cu_q, cu_seqlens_k=dw.cu_k, kv_valid_len=dw.vl,
+                         kind=wl.kind, mask_params=dw.mask_params, softmax_scale=wl.scale,
+                         err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     host = [t.float().cpu().numpy().astype(np.float64) for t in grads]
@@ -78,3 +80,25 @@ def test_bwd_full_size_sampled(cfg):
         c0 = n * wl.tile_n
         _close(dk[b, c0:c0 + rk.shape[0], h], rk, f"dk h={h} n={n}")
         _close(dv[b, c0:c0 + rv.shape[0], h], rv, f"dv h={h} n={n}")
+
+
+def test_bwd_varlen_workload_sampled():
+    wl = make_workload(3)
+    (q, k, v, g), (dq, dk, dv) = _run(wl)
+    assert all(np.all(np.isfinite(t)) for t in (dq, dk, dv))
+    meta = oracle.build_meta(wl)
+    rng = np.random.default_rng(703)
+    picks = [int(rng.integers(wl.B)) for _ in range(4)] + [wl.B - 1]
+    for j, b in enumerate(picks):
+        view, mb, qs, ks = oracle.seq_view(wl, meta, b)
+        qb, kb, vb, gb = q[qs][None], k[ks][None], v[ks][None], g[qs][None]
+        h = int(rng.integers(wl.H))
+        m = view.num_m - 1 if j == len(picks) - 1 else int(rng.integers(view.num_m))
+        n = view.num_n - 1 if j == len(picks) - 1 else int(rng.integers(view.num_n))
+        ref = oracle.bwd_dq_tile(view, qb, kb, vb, gb, mb, 0, h, m)
+        r0 = qs.start + m * wl.tile_m
+        _close(dq[r0:r0 + ref.shape[0], h], ref, f"dq b={b} h={h} m={m}")
+        rk, rv = oracle.bwd_dkdv_tile(view, qb, kb, vb, gb, mb, 0, h, n)
+        c0 = ks.start + n * wl.tile_n
+        _close(dk[c0:c0 + rk.shape[0], h], rk, f"dk b={b} h={h} n={n}")
+        _close(dv[c0:c0 + rv.shape[0], h], rv, f"dv b={b} h={h} n={n}")

@@ -101,3 +101,62 @@ def test_per_tile_backward_equals_the_dense_one(c):
                 c0 = n * wl.tile_n
                 assert np.max(np.abs(tk - dk[b, c0:c0 + tk.shape[0], h]), initial=0) < 1e-12
                 assert np.max(np.abs(tv - dv[b, c0:c0 + tv.shape[0], h]), initial=0) < 1e-12
+
+
+VARLEN_CASES = [
+    dict(seed=211, B=3, H=2, D=8, seqlens_q=[300, 129, 200], seqlens_k=[260, 400, 128],
+         varlen=True, kind=MASK_CAUSAL),
+    dict(seed=212, B=3, H=1, D=8, seqlens_q=[250, 90, 310], varlen=True,
+         kind=MASK_SLIDING_WINDOW, window_left=100, sink_tokens=30, valid_len=True),
+    dict(seed=213, B=2, H=2, D=8, seqlens_q=[280, 170], varlen=True, kind=MASK_DOCUMENT,
+         density=0.7),
+    dict(seed=214, B=2, H=1, D=8, seqlens_q=[200, 330], seqlens_k=[310, 150], varlen=True,
+         kind=MASK_PREFIX, prefix_len=140, valid_len=True),
+]
+
+
+@pytest.mark.parametrize("c", VARLEN_CASES)
+def test_sequence_views_reproduce_the_c_oracle_varlen_forward(c):
+    # each sequence of a varlen workload, taken as a batched workload of one with
+    # its slice of the packed lists, gives the C oracle's varlen forward rows
+    wl = random_workload(**c)
+    q, k, v = wl.qkv()
+    meta = oracle.build_meta(wl)
+    o_c, _ = oracle.fwd(wl, q, k, v, meta)
+    for b in range(wl.B):
+        view, mb, qs, ks = oracle.seq_view(wl, meta, b)
+        o = oracle.fwd_f64(view, mb, _w(q[qs])[None], _w(k[ks])[None], _w(v[ks])[None])[0]
+        assert np.max(np.abs(o - o_c[qs])) < 1e-12
+
+
+@pytest.mark.parametrize("c", VARLEN_CASES[:2])
+def test_varlen_gradients_match_finite_differences(c):
+    wl = random_workload(**c)
+    q, k, v = wl.qkv()
+    meta = oracle.build_meta(wl)
+    rng = np.random.default_rng(c["seed"])
+    g_bits = wl.tensor("do")
+    dq, dk, dv = oracle.bwd(wl, q, k, v, meta, g_bits)
+    G = _w(g_bits)
+    qf, kf, vf = _w(q), _w(k), _w(v)
+
+    def loss(qq, kk, vv):
+        tot = 0.0
+        for b in range(wl.B):
+            view, mb, qs, ks = oracle.seq_view(wl, meta, b)
+            o = oracle.fwd_f64(view, mb, qq[qs][None], kk[ks][None], vv[ks][None])[0]
+            tot += float((o * G[qs]).sum())
+        return tot
+
+    eps = 1e-6
+    for name, x, grad in (("q", qf, dq), ("k", kf, dk), ("v", vf, dv)):
+        for _ in range(4):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            a_p = {"q": qf, "k": kf, "v": vf}
+            a_m = dict(a_p)
+            a_p[name], a_m[name] = xp, xm
+            fd = (loss(a_p["q"], a_p["k"], a_p["v"]) - loss(a_m["q"], a_m["k"], a_m["v"])) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx)
