@@ -368,11 +368,12 @@ struct BwdCfg {
     static constexpr uint32_t kSt = 2 * kTileBytes;           // stage s: kSt + s * 2 * kTileBytes
     static constexpr uint32_t kVec = kSt + 4 * kTileBytes;   // stage s: 2 x 128 floats at kVec + 1024 s
     static constexpr uint32_t kBar = kVec + 2048;
-    // barriers: resident tiles full, stage full [2], stage empty [2], S and dP
+    // barriers: resident tiles full, stage full [2] (dQ kernel: its first tile,
+    // K), stage second tile full [2] (dQ kernel: V), stage empty [2], S and dP
     // ready (first / second half of the tile), elementwise done (first / second
     // half), accumulators done, MMA drain
-    static constexpr int bRF = 0, bF = 1, bE = 3, bSR = 5, bSR2 = 6, bPR = 7, bPR2 = 8, bDone = 9;
-    static constexpr int bDrain = 10, kNumBars = 11;
+    static constexpr int bRF = 0, bF = 1, bF2 = 3, bE = 5, bSR = 7, bSR2 = 8, bPR = 9, bPR2 = 10;
+    static constexpr int bDone = 11, bDrain = 12, kNumBars = 13;
     static constexpr uint32_t kInfo = kBar + kNumBars * 8;    // int32 [2][4]
     static constexpr uint32_t kMisc = kInfo + 32;             // [0] tmem base, [1] abort
     static constexpr uint32_t kBytes = kMisc + 16;
@@ -399,6 +400,7 @@ __device__ __forceinline__ void bwd_init(uint8_t *gbase, uint32_t base, uint32_t
         mbar_init(bar(C::bRF), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(C::bF + s), 1);
+            mbar_init(bar(C::bF2 + s), 1);
             mbar_init(bar(C::bE + s), 1);
         }
         mbar_init(bar(C::bSR), 1);
@@ -781,43 +783,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             info[s * 4 + 1] = e < cm ? 1 : 0;
             const int kvrow = (int)(sg.k0 + n * kTile);
             const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
-            mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), 2 * C::kTileBytes);
-            for (int x = 0; x < C::kSub; ++x) {
+            // K first on its own barrier (S needs it), then V (dP needs it)
+            mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), C::kTileBytes);
+            for (int x = 0; x < C::kSub; ++x)
                 tma_load_3d_lead(lead, st + x * C::kSubBytes, &tk, bar(C::bF + s), x * 64, h, kvrow);
-                tma_load_3d_lead(lead, st + C::kTileBytes + x * C::kSubBytes, &tv, bar(C::bF + s), x * 64, h,
+            mbar_arrive_expect_tx_lead(lead, bar(C::bF2 + s), C::kTileBytes);
+            for (int x = 0; x < C::kSub; ++x)
+                tma_load_3d_lead(lead, st + C::kTileBytes + x * C::kSubBytes, &tv, bar(C::bF2 + s), x * 64, h,
                                  kvrow);
-            }
             ++it;
         }
         mbar_wait_drain(bar(C::bRF), 0);
         for (int s = 0; s < 2; ++s) {
             const int uses = (it + 1 - s) / 2;
-            if (uses > 0) mbar_wait_drain(bar(C::bF + s), (uint32_t)(uses - 1) & 1u);
+            if (uses > 0) {
+                mbar_wait_drain(bar(C::bF + s), (uint32_t)(uses - 1) & 1u);
+                mbar_wait_drain(bar(C::bF2 + s), (uint32_t)(uses - 1) & 1u);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMAs --
-        // Per listed KV tile, in two key halves h (N = 64): S_h, dP_h -> SR_h; after
-        // PR_h, half h of the next tile's S and dP, then dQ += dS_h K_h of this one.
+        // Per listed KV tile, in two key halves h (N = 64): S_h, dP_h -> SR_h.  After
+        // PR_h of tile t: dQ += dS_h K_h of tile t, then half h of tile t + 1 (its
+        // first half waits for K and then V of tile t + 1, so the dQ product runs
+        // while they land).
         constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 64, false);
         constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dQk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dOk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        auto issue_s = [&](int s, int half) {  // S_h = Q K_h^T, dP_h = dO V_h^T (rows 64 h.. of the stage)
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u;
-            const uint64_t dKk = smem_desc_sw128(st, 16, 1024);
-            const uint64_t dVk = smem_desc_sw128(st + C::kTileBytes, 16, 1024);
+        // S_h = Q K_h^T (rows 64 h.. of the stage's K), or dP_h = dO V_h^T
+        auto issue_mm = [&](int s, int half, bool dp) {
+            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u +
+                                (dp ? C::kTileBytes : 0u);
+            const uint64_t dB = smem_desc_sw128(st, 16, 1024);
+            const uint64_t dA = dp ? dOk : dQk;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tS + 64u * half, dQk + off, dKk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, (dp ? tP : tS) + 64u * half, dA + off, dB + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tP + 64u * half, dOk + off, dVk + off, idesc_ss, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_lead(lead, bar(half ? C::bSR2 : C::bSR));
         };
         auto issue_dq = [&](int s, int half, int it) {  // dQ += dS_h K_h (16 keys per step)
             const uint64_t dKm = smem_desc_sw128(base + C::kSt + (uint32_t)s * 2u * C::kTileBytes, C::kSubBytes, 1024);
@@ -826,14 +831,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ts_lead(lead, tdQ, tDS + 64u * s + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
                             (it > 0 || kk > 0) ? 1u : 0u);
         };
+        // first half of the tile in stage s, use u: S after K lands, dP after V lands
+        auto first_half = [&](int s, int u) -> bool {
+            if (!mbar_wait(bar(C::bF + s), u & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) return false;
+            tc_fence_after();
+            issue_mm(s, 0, false);
+            if (!mbar_wait(bar(C::bF2 + s), u & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) return false;
+            tc_fence_after();
+            issue_mm(s, 0, true);
+            mma_commit_lead(lead, bar(C::bSR));
+            return true;
+        };
         bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
         tc_fence_after();
         if (ok && total > 0) {
-            ok = mbar_wait(bar(C::bF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            tc_fence_after();
-            if (ok) {
-                issue_s(0, 0);
-                issue_s(0, 1);
+            if ((ok = first_half(0, 0))) {
+                issue_mm(0, 1, false);
+                issue_mm(0, 1, true);
+                mma_commit_lead(lead, bar(C::bSR2));
             }
         }
         for (int it = 0; ok && it < total; ++it) {
@@ -841,17 +856,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool more = it + 1 < total;
             if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
-            if (more) {
-                if (!(ok = mbar_wait(bar(C::bF + (s ^ 1)), ((it + 1) >> 1) & 1, abort_flag, p.err,
-                                     BSATTN_FLAG_TIMEOUT)))
-                    break;
-                tc_fence_after();
-                issue_s(s ^ 1, 0);
-            }
             issue_dq(s, 0, it);
+            if (more && !(ok = first_half(s ^ 1, (it + 1) >> 1))) break;
             if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
-            if (more) issue_s(s ^ 1, 1);
+            if (more) {
+                issue_mm(s ^ 1, 1, false);
+                issue_mm(s ^ 1, 1, true);
+                mma_commit_lead(lead, bar(C::bSR2));
+            }
             issue_dq(s, 1, it);
             mma_commit_lead(lead, bar(C::bE + s));
         }
