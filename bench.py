@@ -63,6 +63,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(pg, ms: float, device) -> float:
+    """The largest of the ranks' timings (ms); `pg` is torch.distributed with an
+    initialised process group, or None for one rank."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flop_per_rank_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes flop_per_rank_step per step
+    (replicas, weak scaling) and the job takes the slowest rank's time."""
+    return world * flop_per_rank_step * steps / (ms * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -490,11 +507,8 @@ def run_native(args):
     total_ms = t_start.elapsed_time(t_end)
     meta_ms = [a.elapsed_time(b) for a, b, _ in ev]
     fwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = ws * flop_step * K / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(pg, total_ms, dev)
+    value = whole_job_tflops(ws, flop_step, K, total_ms)
 
     # ------------------------------------------------------- end-to-end leg
     # Every step copies its inputs in from pinned host memory and its O / LSE back
@@ -563,15 +577,11 @@ def run_native(args):
     s_out.wait_stream(s_cmp)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + hmap.numel() + (
         hvl.numel() * 4 if hvl is not None else 0)
     d2h = out.numel() * 2 + lse.numel() * 4
-    e2e_value = ws * flop_step * K / (e2e_ms * 1e-3) / 1e12
+    e2e_value = whole_job_tflops(ws, flop_step, K, e2e_ms)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())}")
     meta_formats = time_meta_formats(wl, dw, meta, err, stream) if not args.no_meta_formats else None
