@@ -518,7 +518,7 @@ def run_native(args):
     # i's compute overlaps step i+1's copy in and step i-1's copy out.  (Spreading
     # the copy-in over three streams measured no faster: the host link, not one
     # copy engine, bounds it: ~212 GB/s host-to-device alone, ~157 GB/s each way
-    # with both directions busy, measured on a GB300 node.)
+    # with both directions busy, as measured.)
     import copy as _copy
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     slots = [dw, _copy.copy(dw)]
