@@ -328,37 +328,79 @@ __global__ void __launch_bounds__(1024) bsattn_bwd_order_kernel(BwdParams p) {
 }
 
 // ------------------------------------------------------------ 2. row pass --
-// One warp per padded query row (Q tile, r): D = sum_d dO O in fp32 and
-// LSE * log2(e).  Rows past the sequence, and rows with no keys (LSE = -inf),
-// get LSE2 = +inf, so every probability they would form is 0.
+// One warp per 4 padded query rows (Q tile, r .. r + 3): D = sum_d dO O in fp32
+// and LSE * log2(e).  Each lane takes D / 32 consecutive elements of every row
+// (one 8- or 4-byte load of dO and one of O per row), the four rows' loads issued
+// before any is used.  Rows past the sequence, and rows with no keys
+// (LSE = -inf), get LSE2 = +inf, so every probability they would form is 0.
+constexpr int kRowsPerWarp = 4;
 __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    const long long row0 = w * kRowsPerWarp;
     int b, h, m;
     Seq s;
-    if (!q_item(p, w / kTile, b, h, m, s)) return;
-    const int i = m * kTile + (int)(w % kTile);
-    float d = 0.f, l2 = INFINITY;
-    if (i < s.sq) {
-        const long long row = (s.q0 + i) * p.H + h;  // packed [rows, H] row
-        for (int c = lane; c < p.D; c += 32) {
-            const float g = __uint_as_float((uint32_t)p.dout[row * p.D + c] << 16);
-            const float o = p.o_f32 ? static_cast<const float *>(p.o)[row * p.D + c]
-                                    : __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.o)[row * p.D + c] << 16);
-            d = fmaf(g, o, d);
+    if (!q_item(p, row0 / kTile, b, h, m, s)) return;
+    const int r0 = (int)(row0 % kTile);
+    const bool wide = p.D == 128;  // 4 elements per lane (else 2)
+    uint2 g[kRowsPerWarp];         // dO, bf16 pairs
+    float4 o[kRowsPerWarp];        // O as fp32
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        const int i = m * kTile + r0 + k;
+        g[k] = make_uint2(0u, 0u);
+        o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i >= s.sq) continue;
+        const long long e = ((s.q0 + i) * p.H + h) * p.D + (long long)lane * (wide ? 4 : 2);
+        if (wide) {
+            g[k] = *reinterpret_cast<const uint2 *>(p.dout + e);
+            if (p.o_f32) {
+                o[k] = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.o) + e);
+            } else {
+                const uint2 ob = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p.o) + e);
+                o[k] = make_float4(__uint_as_float(ob.x << 16), __uint_as_float(ob.x & 0xffff0000u),
+                                   __uint_as_float(ob.y << 16), __uint_as_float(ob.y & 0xffff0000u));
+            }
+        } else {
+            g[k].x = *reinterpret_cast<const uint32_t *>(p.dout + e);
+            if (p.o_f32) {
+                const float2 of = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.o) + e);
+                o[k] = make_float4(of.x, of.y, 0.f, 0.f);
+            } else {
+                const uint32_t ob = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(p.o) + e);
+                o[k] = make_float4(__uint_as_float(ob << 16), __uint_as_float(ob & 0xffff0000u), 0.f, 0.f);
+            }
         }
-        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        const long long li = p.varlen ? (long long)h * p.rows_q + s.q0 + i : ((long long)b * p.H + h) * s.sq + i;
-        const float lse = p.lse[li];
-        l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
     }
-    if (lane == 0) {
-        const long long at = vec_at(p, s, b, h, m) + (w % kTile);
-        p.dvec[at] = d;
+    float d[kRowsPerWarp];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        float acc = __uint_as_float(g[k].x << 16) * o[k].x;
+        acc = fmaf(__uint_as_float(g[k].x & 0xffff0000u), o[k].y, acc);
+        acc = fmaf(__uint_as_float(g[k].y << 16), o[k].z, acc);
+        acc = fmaf(__uint_as_float(g[k].y & 0xffff0000u), o[k].w, acc);
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        d[k] = acc;
+    }
+    if (lane < kRowsPerWarp) {  // lane k writes row r0 + k
+        const int i = m * kTile + r0 + lane;
+        float dk = 0.f, l2 = INFINITY;
+#pragma unroll
+        for (int k = 0; k < kRowsPerWarp; ++k)
+            if (k == lane) dk = d[k];
+        if (i < s.sq) {
+            const long long li = p.varlen ? (long long)h * p.rows_q + s.q0 + i : ((long long)b * p.H + h) * s.sq + i;
+            const float lse = p.lse[li];
+            l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+        }
+        const long long at = vec_at(p, s, b, h, m) + r0 + lane;
+        p.dvec[at] = dk;
         p.lse2[at] = l2;
     }
 }
 
+// Shared memory of both gradient kernels: two resident tiles, a ring of two
+// stages of two tiles plus two 128-float vectors, barriers, item info, misc.
 template <int D>
 struct BwdCfg {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
@@ -1014,7 +1056,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
     bsattn_bwd_order_kernel<<<1, 1024, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (q_tiles > 0) {
-        bsattn_bwd_rows_kernel<<<warp_blocks(q_tiles * kTile), 256, 0, stream>>>(p);
+        bsattn_bwd_rows_kernel<<<warp_blocks(q_tiles * kTile / kRowsPerWarp), 256, 0, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // every KV tile writes its dK / dV rows (zeros without listed Q tiles)
