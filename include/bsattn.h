@@ -1,5 +1,7 @@
 /*
- * bsattn -- block-sparse attention forward for NVIDIA GB300 (sm_103a).
+ * bsattn -- block-sparse attention for NVIDIA GB300 (sm_103a): metadata from a
+ * block map (byte map, bitmask, BSR or coarse blocks), the forward (exact, or
+ * with proxy compensation), and the backward of the exact forward.
  *
  * C ABI.  Every pointer argument is caller-owned memory; the library allocates
  * nothing and keeps no state between calls.  Device pointers must be CUDA
@@ -24,6 +26,12 @@
  *  - "[feat] VSA-256 fastpath on Blackwell via FA4 CuTe block-sparse
  *    attention" (FastVideo #1354): Q/K/V in BSHD layout; a per-KV-block valid
  *    length read by mask_mod; LSE in [B, H, S] layout.
+ *  - "feat(prims-ts): support proxy-compensated block-sparse attention"
+ *    (FlashInfer #4872): the bitmask and BSR selection formats and proxy
+ *    compensation (see bsattn_build_meta_bitmask, bsattn_build_meta_bsr,
+ *    bsattn_fwd_proxy).
+ *  The backward (bsattn_bwd) is the gradient of the forward's definition; the
+ *  first two pages name it as the missing step for training.
  */
 #ifndef BSATTN_H
 #define BSATTN_H
