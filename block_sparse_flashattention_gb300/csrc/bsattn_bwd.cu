@@ -758,11 +758,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// Shared memory of the dQ kernel: Q and dO resident, a ring of three K tiles and
+// one of two V tiles (V is done with one item earlier than K: after the item's
+// dP products, K only after its dQ products), barriers, item info, misc.
+template <int D>
+struct DqCfg {
+    static constexpr uint32_t kTileBytes = kTile * D * 2;
+    static constexpr int kSub = D / 64;
+    static constexpr uint32_t kSubBytes = kTile * 64 * 2;
+    static constexpr int kKStages = 3, kVStages = 2;
+    static constexpr uint32_t kRes0 = 0, kRes1 = kTileBytes;     // Q, dO
+    static constexpr uint32_t kK = 2 * kTileBytes;               // K stage s at kK + s * kTileBytes
+    static constexpr uint32_t kV = kK + kKStages * kTileBytes;   // V stage s at kV + s * kTileBytes
+    static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
+    // barriers: resident tiles, K full [3], K empty [3], V full [2], V empty [2],
+    // S and dP ready (two halves), dS done (two halves), dQ done, MMA drain
+    static constexpr int bRF = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSR = 11, bSR2 = 12, bPR = 13;
+    static constexpr int bPR2 = 14, bDone = 15, bDrain = 16, kNumBars = 17;
+    static constexpr uint32_t kInfo = kBar + kNumBars * 8;       // int32 [3][2]: tile, mask flag
+    static constexpr uint32_t kMisc = kInfo + 32;                // [0] tmem base, [1] abort
+    static constexpr uint32_t kBytes = kMisc + 16;
+    static constexpr uint32_t kSmemAlloc = kBytes + 1024;        // slack for 1024-byte alignment
+};
+
+template <int D>
+__device__ __forceinline__ void dq_init(uint8_t *gbase, uint32_t base, uint32_t warp) {
+    using C = DqCfg<D>;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + C::kMisc);
+    auto bar = [&](int i) -> uint32_t { return base + C::kBar + 8u * (uint32_t)i; };
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::bRF), 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(bar(C::bKF + s), 1);
+            mbar_init(bar(C::bKE + s), 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(bar(C::bVF + s), 1);
+            mbar_init(bar(C::bVE + s), 1);
+        }
+        mbar_init(bar(C::bSR), 1);
+        mbar_init(bar(C::bSR2), 1);
+        mbar_init(bar(C::bPR), kEwWarps);
+        mbar_init(bar(C::bPR2), kEwWarps);
+        mbar_init(bar(C::bDone), 1);
+        mbar_init(bar(C::bDrain), 1);
+        misc[1] = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 2) {
+        tmem_alloc(base + C::kMisc, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
 // ------------------------------------------------------------------ 5. dQ --
 // One CTA per (b, h, Q tile m), 384 threads, the same roles: Q and dO of the
 // tile stay resident, K and V of each listed KV tile (the forward's mask list,
 // then its full list; entries outside [0, num_n) skipped by every role alike)
-// pass through the two-stage ring.  Thread = query row; column group cg of the
+// pass through the K and V rings.  Thread = query row; column group cg of the
 // elementwise warps takes key chunk 2 h + cg of key half h.
 // TMEM: S [0, 128), dP [128, 256), dS buffers (bf16) [256, 320) and [320, 384),
 // dQ [384, 384 + D).  S and dP are formed in two key halves; half h of tile t + 1
@@ -774,7 +831,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                          const __grid_constant__ CUtensorMap tdo) {
-    using C = BwdCfg<D>;
+    using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -803,7 +860,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         total += __popc(__ballot_sync(0xffffffffu, e < cm + cf && entry(e) >= 0));
     }
 
-    bwd_init<D>(gbase, base, warp);
+    dq_init<D>(gbase, base, warp);
     const uint32_t tmem = misc[0];
     const uint32_t tS = tmem, tP = tmem + 128u, tDS = tmem + 256u, tdQ = tmem + 384u;
 
@@ -815,33 +872,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d_lead(lead, base + C::kRes0 + x * C::kSubBytes, &tq, bar(C::bRF), x * 64, h, qrow);
             tma_load_3d_lead(lead, base + C::kRes1 + x * C::kSubBytes, &tdo, bar(C::bRF), x * 64, h, qrow);
         }
-        int it = 0;
+        int nk = 0, nv = 0;  // K and V tiles issued
         for (int e = 0; e < cm + cf; ++e) {
             const int n = entry(e);
             if (n < 0) continue;
-            const int s = it & 1;
-            if (!mbar_wait(bar(C::bE + s), ((it >> 1) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
-            info[s * 4 + 0] = n;
-            info[s * 4 + 1] = e < cm ? 1 : 0;
+            const int ks = nk % C::kKStages, vs = nv % C::kVStages;
             const int kvrow = (int)(sg.k0 + n * kTile);
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
-            // K first on its own barrier (S needs it), then V (dP needs it)
-            mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), C::kTileBytes);
+            // K first (S needs it), then V (dP needs it), each on its own ring
+            if (!mbar_wait(bar(C::bKE + ks), ((nk / C::kKStages) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                break;
+            info[ks * 2 + 0] = n;
+            info[ks * 2 + 1] = e < cm ? 1 : 0;
+            mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
             for (int x = 0; x < C::kSub; ++x)
-                tma_load_3d_lead(lead, st + x * C::kSubBytes, &tk, bar(C::bF + s), x * 64, h, kvrow);
-            mbar_arrive_expect_tx_lead(lead, bar(C::bF2 + s), C::kTileBytes);
+                tma_load_3d_lead(lead, base + C::kK + ks * C::kTileBytes + x * C::kSubBytes, &tk, bar(C::bKF + ks),
+                                 x * 64, h, kvrow);
+            ++nk;
+            if (!mbar_wait(bar(C::bVE + vs), ((nv / C::kVStages) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                break;
+            mbar_arrive_expect_tx_lead(lead, bar(C::bVF + vs), C::kTileBytes);
             for (int x = 0; x < C::kSub; ++x)
-                tma_load_3d_lead(lead, st + C::kTileBytes + x * C::kSubBytes, &tv, bar(C::bF2 + s), x * 64, h,
-                                 kvrow);
-            ++it;
+                tma_load_3d_lead(lead, base + C::kV + vs * C::kTileBytes + x * C::kSubBytes, &tv, bar(C::bVF + vs),
+                                 x * 64, h, kvrow);
+            ++nv;
         }
         mbar_wait_drain(bar(C::bRF), 0);
-        for (int s = 0; s < 2; ++s) {
-            const int uses = (it + 1 - s) / 2;
-            if (uses > 0) {
-                mbar_wait_drain(bar(C::bF + s), (uint32_t)(uses - 1) & 1u);
-                mbar_wait_drain(bar(C::bF2 + s), (uint32_t)(uses - 1) & 1u);
-            }
+        for (int s = 0; s < C::kKStages; ++s) {
+            const int uses = (nk + C::kKStages - 1 - s) / C::kKStages;
+            if (uses > 0) mbar_wait_drain(bar(C::bKF + s), (uint32_t)(uses - 1) & 1u);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            const int uses = (nv + C::kVStages - 1 - s) / C::kVStages;
+            if (uses > 0) mbar_wait_drain(bar(C::bVF + s), (uint32_t)(uses - 1) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMAs --
@@ -854,10 +916,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dQk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dOk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        // S_h = Q K_h^T (rows 64 h.. of the stage's K), or dP_h = dO V_h^T
-        auto issue_mm = [&](int s, int half, bool dp) {
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u +
-                                (dp ? C::kTileBytes : 0u);
+        // S_h = Q K_h^T (rows 64 h.. of the item's K stage), or dP_h = dO V_h^T
+        auto issue_mm = [&](int it, int half, bool dp) {
+            const uint32_t st = base + (dp ? C::kV + (uint32_t)(it % C::kVStages) * C::kTileBytes
+                                           : C::kK + (uint32_t)(it % C::kKStages) * C::kTileBytes) +
+                                (uint32_t)half * 8192u;
             const uint64_t dB = smem_desc_sw128(st, 16, 1024);
             const uint64_t dA = dp ? dOk : dQk;
 #pragma unroll
@@ -866,49 +929,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ss_lead(lead, (dp ? tP : tS) + 64u * half, dA + off, dB + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_dq = [&](int s, int half, int it) {  // dQ += dS_h K_h (16 keys per step)
-            const uint64_t dKm = smem_desc_sw128(base + C::kSt + (uint32_t)s * 2u * C::kTileBytes, C::kSubBytes, 1024);
+        auto issue_dq = [&](int it, int half) {  // dQ += dS_h K_h (16 keys per step)
+            const uint64_t dKm =
+                smem_desc_sw128(base + C::kK + (uint32_t)(it % C::kKStages) * C::kTileBytes, C::kSubBytes, 1024);
 #pragma unroll
             for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
-                mma_ts_lead(lead, tdQ, tDS + 64u * s + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)), idesc_ts,
-                            (it > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_lead(lead, tdQ, tDS + 64u * (uint32_t)(it & 1) + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)),
+                            idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
         };
-        // first half of the tile in stage s, use u: S after K lands, dP after V lands
-        auto first_half = [&](int s, int u) -> bool {
-            if (!mbar_wait(bar(C::bF + s), u & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) return false;
+        // first half of item it: S after its K lands, dP after its V lands
+        auto first_half = [&](int it) -> bool {
+            if (!mbar_wait(bar(C::bKF + it % C::kKStages), (it / C::kKStages) & 1, abort_flag, p.err,
+                           BSATTN_FLAG_TIMEOUT))
+                return false;
             tc_fence_after();
-            issue_mm(s, 0, false);
-            if (!mbar_wait(bar(C::bF2 + s), u & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) return false;
+            issue_mm(it, 0, false);
+            if (!mbar_wait(bar(C::bVF + it % C::kVStages), (it / C::kVStages) & 1, abort_flag, p.err,
+                           BSATTN_FLAG_TIMEOUT))
+                return false;
             tc_fence_after();
-            issue_mm(s, 0, true);
+            issue_mm(it, 0, true);
             mma_commit_lead(lead, bar(C::bSR));
             return true;
         };
+        // second half of item it; its V stage is free once these have read it
+        auto second_half = [&](int it) {
+            issue_mm(it, 1, false);
+            issue_mm(it, 1, true);
+            mma_commit_lead(lead, bar(C::bSR2));
+            mma_commit_lead(lead, bar(C::bVE + it % C::kVStages));
+        };
         bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
         tc_fence_after();
-        if (ok && total > 0) {
-            if ((ok = first_half(0, 0))) {
-                issue_mm(0, 1, false);
-                issue_mm(0, 1, true);
-                mma_commit_lead(lead, bar(C::bSR2));
-            }
-        }
+        if (ok && total > 0 && (ok = first_half(0))) second_half(0);
         for (int it = 0; ok && it < total; ++it) {
-            const int s = it & 1;
             const bool more = it + 1 < total;
             if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
-            issue_dq(s, 0, it);
-            if (more && !(ok = first_half(s ^ 1, (it + 1) >> 1))) break;
+            issue_dq(it, 0);
+            if (more && !(ok = first_half(it + 1))) break;
             if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
             tc_fence_after();
-            if (more) {
-                issue_mm(s ^ 1, 1, false);
-                issue_mm(s ^ 1, 1, true);
-                mma_commit_lead(lead, bar(C::bSR2));
-            }
-            issue_dq(s, 1, it);
-            mma_commit_lead(lead, bar(C::bE + s));
+            if (more) second_half(it + 1);
+            issue_dq(it, 1);
+            mma_commit_lead(lead, bar(C::bKE + it % C::kKStages));  // K stage free once these have read it
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
         mma_commit_lead(lead, bar(C::bDrain));
@@ -926,12 +990,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int32_t dqid = (p.kind == BSATTN_MASK_DOCUMENT && i < sg.sq) ? p.doc_q[sg.q0 + i] : 0;
         bool ok = true;
         for (int it = 0; it < total; ++it) {
-            const int s = it & 1;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err,
-                                                         BSATTN_FLAG_TIMEOUT))))
+            const int s = it & 1;            // dS buffer
+            const int ks = it % C::kKStages;  // K stage (item info)
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bKF + ks), (it / C::kKStages) & 1, abort_flag,
+                                                         p.err, BSATTN_FLAG_TIMEOUT))))
                 break;
-            const int n = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 0];
-            const bool msk = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 1] != 0;
+            const int n = reinterpret_cast<volatile int32_t *>(info)[ks * 2 + 0];
+            const bool msk = reinterpret_cast<volatile int32_t *>(info)[ks * 2 + 1] != 0;
             int lim = min(kTile, sg.sk - n * kTile);
             if (msk && p.vl) lim = min(lim, __ldg(p.vl + (long long)b * p.num_n + n));
             // kept key columns: span [lo0, hi0) plus span [lo1, hi1), cut to [0, lim)
@@ -1012,6 +1077,11 @@ template <int D>
 constexpr uint32_t bwd_smem_bytes() {
     return BwdCfg<D>::kSmemAlloc > 120u * 1024u ? BwdCfg<D>::kSmemAlloc : 120u * 1024u;
 }
+template <int D>
+constexpr uint32_t dq_smem_bytes() {
+    return DqCfg<D>::kSmemAlloc > 120u * 1024u ? DqCfg<D>::kSmemAlloc : 120u * 1024u;
+}
+static_assert(DqCfg<128>::kSmemAlloc <= 232448u, "dQ kernel shared memory exceeds 227 KB");
 
 template <int D>
 cudaError_t prepare_bwd_kernels() {
@@ -1025,7 +1095,7 @@ cudaError_t prepare_bwd_kernels() {
                                  (int)bwd_smem_bytes<D>());
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(bsattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bwd_smem_bytes<D>());
+                                 (int)dq_smem_bytes<D>());
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
@@ -1063,7 +1133,7 @@ cudaError_t launch_bwd_d(const BwdParams &p, const CUtensorMap &tq, const CUtens
     bsattn_bwd_dkdv_kernel<D><<<(unsigned)kv_items, kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (q_tiles > 0)
-        bsattn_bwd_dq_kernel<D><<<(unsigned)q_tiles, kBwdThreads, bwd_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
+        bsattn_bwd_dq_kernel<D><<<(unsigned)q_tiles, kBwdThreads, dq_smem_bytes<D>(), stream>>>(p, tq, tk, tv, tdo);
     return cudaGetLastError();
 }
 
