@@ -105,9 +105,11 @@ struct Cfg {
     static constexpr uint32_t kK = kQ + 2 * kTileBytes;
     static constexpr uint32_t kV = kK + kStagesK * kTileBytes;
     static constexpr uint32_t kBar = kV + kStagesV * kTileBytes;
-    // barrier indices
-    static constexpr int bKF = 0, bKE = kStagesK, bVF = 2 * kStagesK, bVE = 2 * kStagesK + kStagesV;
-    static constexpr int bQF = 2 * kStagesK + 2 * kStagesV, bQE = bQF + 2, bSR = bQF + 4,
+    // barrier indices.  bKF + s completes when item s's K tile and its V tile have
+    // both landed (one wait per item covers both loads); bKE / bVE release the
+    // K and V stages.
+    static constexpr int bKF = 0, bKE = kStagesK, bVE = 2 * kStagesK;
+    static constexpr int bQF = 2 * kStagesK + kStagesV, bQE = bQF + 2, bSR = bQF + 4,
                          bPR = bQF + 6,  // bPR + 2t + half
                          bED = bQF + 10, bUF = bQF + 12, bUE = bQF + 14, bDrain = bQF + 16,
                          kNumBars = bQF + 17;
@@ -247,10 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::bKF + s), 1);
             mbar_init(bar(C::bKE + s), 1);
         }
-        for (int s = 0; s < C::kStagesV; ++s) {
-            mbar_init(bar(C::bVF + s), 1);
-            mbar_init(bar(C::bVE + s), 1);
-        }
+        for (int s = 0; s < C::kStagesV; ++s) mbar_init(bar(C::bVE + s), 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(C::bQF + t), 1);
             mbar_init(bar(C::bQE + t), 1);
@@ -386,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p0) it.lim0 = min(min(kTile, ti[0].sk - c0 * kTile), vl0);
                     if (p1) it.lim1 = min(min(kTile, ti[1].sk - c1 * kTile), vl1);
                     items[ks] = it;
-                    mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
+                    // K and V of the item complete one barrier (V lands in its own ring).
+                    mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), 2 * C::kTileBytes);
                     for (int x = 0; x < C::kSub; ++x)
                         tma_load_3d_lead(lead, sK + ks * C::kTileBytes + x * kSubTileBytes, &tk, bar(C::bKF + ks),
                                     x * 64, h, it.krow);
@@ -395,9 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
                                    BSATTN_FLAG_TIMEOUT))
                         goto producer_done;
-                    mbar_arrive_expect_tx_lead(lead, bar(C::bVF + vs), C::kTileBytes);
                     for (int x = 0; x < C::kSub; ++x)
-                        tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bVF + vs),
+                        tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bKF + ks),
                                     x * 64, h, it.krow);
                     ++vc;
                 }
@@ -426,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        BSATTN_FLAG_TIMEOUT))
                             goto producer_done;
                         items[ks] = it;
-                        mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
+                        mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), 2 * C::kTileBytes);
                         for (int x = 0; x < C::kSub; ++x)
                             tma_load_3d_lead(lead, sK + ks * C::kTileBytes + x * kSubTileBytes, &tks,
                                              bar(C::bKF + ks), x * 64, h, it.krow);
@@ -435,10 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
                                        BSATTN_FLAG_TIMEOUT))
                             goto producer_done;
-                        mbar_arrive_expect_tx_lead(lead, bar(C::bVF + vs), C::kTileBytes);
                         for (int x = 0; x < C::kSub; ++x)
                             tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tvs,
-                                             bar(C::bVF + vs), x * 64, h, it.krow);
+                                             bar(C::bKF + ks), x * 64, h, it.krow);
                         ++vc;
                     }
                 }
@@ -477,13 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer_done:
             // Make sure no TMA write into this CTA's shared memory is still in flight.
             // Stage s was last used by item (kc - 1 - s) / kStages * kStages + s, whose
-            // phase is (kc - 1 - s) / kStages.
+            // phase is (kc - 1 - s) / kStages; its barrier also counts that item's V tile.
 #pragma unroll
             for (uint32_t s = 0; s < (uint32_t)C::kStagesK; ++s)
                 if (kc > s) mbar_wait_drain(bar(C::bKF + s), ((kc - 1 - s) / C::kStagesK) & 1u);
-#pragma unroll
-            for (uint32_t s = 0; s < (uint32_t)C::kStagesV; ++s)
-                if (vc > s) mbar_wait_drain(bar(C::bVF + s), ((vc - 1 - s) / C::kStagesV) & 1u);
             if (qn0 > 0) mbar_wait_drain(bar(C::bQF + 0), (qn0 - 1) & 1u);
             if (qn1 > 0) mbar_wait_drain(bar(C::bQF + 1), (qn1 - 1) & 1u);
         }
@@ -519,13 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // could run two phases ahead of this wait); the first four K steps go out
             // as soon as the first half is in TMEM.
             auto issue_pv = [&](int t) -> bool {
-                if (!mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                // Each softmax warp arrives on the first-half barrier before the second,
+                // so a completed second half implies a completed first half: one test
+                // then covers both (the common case when the MMA warp runs behind).
+                const bool both = mbar_test_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1);
+                if (!both &&
+                    !mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
                     return false;
-                const uint32_t vcx = (uint32_t)pend[t];
-                const uint32_t vs = vcx % C::kStagesV;
-                if (!mbar_wait(bar(C::bVF + vs), (vcx / C::kStagesV) & 1, abort_flag, p.err,
-                               BSATTN_FLAG_TIMEOUT))
-                    return false;
+                // The item's V tile landed before its K-stage wait completed.
+                const uint32_t vs = (uint32_t)pend[t] % C::kStagesV;
                 tc_fence_after();
                 const uint64_t vdesc = desc_v + vs * kTileUnits;
                 const uint32_t o_tmem = tmem + 256 + t * D, p_tmem = tmem + t * 128;
@@ -534,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 32; ++kk)
                     mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                            kk > 0 ? 1u : acc0);
-                if (!mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
-                               BSATTN_FLAG_TIMEOUT))
+                if (!both && !mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
+                                        BSATTN_FLAG_TIMEOUT))
                     return false;
                 ++pc[t];
                 tc_fence_after();
