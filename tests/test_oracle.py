@@ -296,6 +296,25 @@ def test_sliding_window_of_one_is_identity():
     assert np.max(np.abs(L - wl.scale * qk)) <= 1e-12
 
 
+@pytest.mark.parametrize("sinks", [5, 130])
+def test_window_of_one_with_sinks_is_library_attention_on_gathered_keys(sinks):
+    """window_left = 1 with s sink tokens: query i sees exactly the keys
+    j < min(s, i + 1) and itself, so each row equals torch SDPA over those keys
+    gathered out of the sequence (s = 130 puts the sink edge inside tile 1)."""
+    wl = random_workload(37, B=1, H=2, D=64, seqlens_q=[300], kind=MASK_SLIDING_WINDOW,
+                         window_left=1, sink_tokens=sinks, density=1.0)
+    q, k, v = wl.qkv()
+    O, L = oracle.fwd(wl, q, k, v, oracle.build_meta(wl))
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    worst_o = worst_l = 0.0
+    for i in range(300):
+        keys = sorted(set(range(min(sinks, i + 1))) | {i})
+        Oi, Li = _sdpa(qf[:, i:i + 1], kf[:, keys], vf[:, keys], wl.scale, False)
+        worst_o = max(worst_o, float(np.max(np.abs(O[:, i:i + 1] - Oi))))
+        worst_l = max(worst_l, float(np.max(np.abs(L[:, :, i:i + 1] - Li))))
+    assert worst_o <= 1e-12 and worst_l <= 1e-12
+
+
 def test_wide_sliding_window_equals_causal_library():
     wl = random_workload(33, B=1, H=2, D=64, seqlens_q=[300], kind=MASK_SLIDING_WINDOW,
                          window_left=10_000, sink_tokens=0, density=1.0)

@@ -16,6 +16,7 @@ from tests import test_oracle as T
 MUTANTS = {
     "causal_strict": ("case KIND_CAUSAL: return j <= i;", "case KIND_CAUSAL: return j < i;"),
     "window_off_by_one": ("i - j < p->window_left", "i - j <= p->window_left"),
+    "sink_off_by_one": ("j < p->sink_tokens", "j <= p->sink_tokens"),
     "prefix_and": ("return j < p->prefix_len || j <= i;", "return j < p->prefix_len && j <= i;"),
     "ascending_lists": ("for (int64_t n = nn - 1; n >= 0; --n) {",
                         "for (int64_t n = 0; n < nn; ++n) {"),
@@ -45,6 +46,7 @@ PINS = [
     (T.test_all_ones_map_equals_library_attention, {"kind": 0, "causal": False}),
     (T.test_all_ones_map_equals_library_attention, {"kind": 1, "causal": True}),
     (T.test_sliding_window_of_one_is_identity, {}),
+    (T.test_window_of_one_with_sinks_is_library_attention_on_gathered_keys, {"sinks": 5}),
     (T.test_prefix_extremes_equal_library, {"prefix": 0, "causal": True}),
     (T.test_valid_length_one_is_strided_library_attention, {}),
     (T.test_partial_tail_tile_never_full, {}),
