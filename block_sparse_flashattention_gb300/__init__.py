@@ -21,12 +21,12 @@ from ._binding import (BSATTN_ERR_CAPACITY, BSATTN_ERR_CUDA, BSATTN_ERR_INVALID_
                        BsattnError, MaskParams, Meta, bsattn_abi_version, bsattn_build_meta,
                        bsattn_build_meta_bitmask, bsattn_build_meta_blocks, bsattn_build_meta_bsr,
                        bsattn_fwd_proxy, bsattn_kv_summaries, bsattn_bwd, bsattn_bwd_workspace_size,
-                       bsattn_fwd, bsattn_fwd_static_scratch, bsattn_fwd_workspace_size, library,
-                       status_string)
+                       bsattn_fwd, bsattn_fwd_static_scratch, bsattn_fwd_workspace_size,
+                       bsattn_testing_set_wait_limit, library, status_string)
 
 TILE = 128
 
-__all__ = ["bsattn_bwd", "bsattn_bwd_workspace_size", "backward", "bsattn_fwd_proxy", "bsattn_kv_summaries", "bsattn_build_meta", "bsattn_build_meta_bitmask", "bsattn_build_meta_blocks", "bsattn_build_meta_bsr", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version",
+__all__ = ["bsattn_bwd", "bsattn_bwd_workspace_size", "backward", "bsattn_fwd_proxy", "bsattn_kv_summaries", "bsattn_build_meta", "bsattn_build_meta_bitmask", "bsattn_build_meta_blocks", "bsattn_build_meta_bsr", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version", "bsattn_testing_set_wait_limit",
            "alloc_meta", "alloc_workspace", "build_meta",
            "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
            "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",

@@ -112,6 +112,8 @@ def library() -> ctypes.CDLL:
         lib.bsattn_status_string.restype = ctypes.c_char_p
         lib.bsattn_abi_version.argtypes = []
         lib.bsattn_abi_version.restype = ctypes.c_int32
+        lib.bsattn_testing_set_wait_limit.argtypes = [ctypes.c_longlong]
+        lib.bsattn_testing_set_wait_limit.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -326,3 +328,11 @@ def bsattn_bwd_workspace_size(meta: Meta) -> int:
 
 def bsattn_abi_version() -> int:
     return int(library().bsattn_abi_version())
+
+
+def bsattn_testing_set_wait_limit(cycles: int) -> None:
+    """Testing hook: pipeline wait limit (SM cycles) of later forward launches;
+    cycles <= 0 restores the default."""
+    st = library().bsattn_testing_set_wait_limit(int(cycles))
+    if st != BSATTN_OK:
+        raise BsattnError(st, "bsattn_testing_set_wait_limit")

@@ -1,5 +1,6 @@
 // C-ABI entry points: host-side validation, TMA tensor maps, kernel launches.
 // Nothing here allocates device memory or synchronises with the device.
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -13,6 +14,9 @@ using bsattn::kTile;
 
 // Workspace: the claim counter in the first 256 bytes, then the unit order.
 constexpr size_t kWorkspaceHeader = 256;
+
+// Pipeline wait limit of the forward launches (0: the default); tests lower it.
+std::atomic<long long> g_wait_limit{0};
 
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -229,6 +233,8 @@ bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, i
     p.out_f32 = out_dtype == BSATTN_OUT_F32 ? 1 : 0;
     p.lse = lse;
     p.err = err_flag;
+    const long long wl = g_wait_limit.load(std::memory_order_relaxed);
+    p.wait_limit = wl > 0 ? wl : bsattn::kDefaultWaitLimitCycles;
     p.pairs_per_head = (int)cdiv(p.total_m, 2);
     if ((long long)H * p.pairs_per_head > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
     p.num_units = H * p.pairs_per_head;
@@ -312,6 +318,11 @@ const char *bsattn_status_string(bsattn_status s) {
 }
 
 int32_t bsattn_abi_version(void) { return BSATTN_ABI_VERSION; }
+
+bsattn_status bsattn_testing_set_wait_limit(long long cycles) {
+    g_wait_limit.store(cycles > 0 ? cycles : 0, std::memory_order_relaxed);
+    return BSATTN_OK;
+}
 
 bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
     if (!bytes) return BSATTN_ERR_INVALID_ARG;
@@ -584,17 +595,44 @@ __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the current device's scratch; resolved once per device, with
-// that device current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+CtxGetCurrentFn get_ctx_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Device address of the current device's scratch.  It is resolved with the
+// device current and kept per CUDA context: a reset device gets a new context
+// (and a new copy of the library's device data), so the address is resolved
+// again after one.
 bsattn_status static_scratch_address(void **addr) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSATTN_ERR_CUDA;
+    CtxGetCurrentFn ctx_fn = get_ctx_fn();
+    if (!ctx_fn) return BSATTN_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (ctx_fn(&ctx) != CUDA_SUCCESS) return BSATTN_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!ctx || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
+        // cudaGetSymbolAddress also makes the device's primary context current on
+        // this thread when none is.
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return BSATTN_ERR_CUDA;
+        if (ctx_fn(&ctx) != CUDA_SUCCESS || !ctx) return BSATTN_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *addr = g_scratch_addr[dev];
     return BSATTN_OK;

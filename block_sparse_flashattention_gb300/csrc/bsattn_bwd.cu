@@ -76,7 +76,9 @@ __device__ __forceinline__ Seq seq_of(const BwdParams &p, int b) {
     s.T0 = p.cu_tm[b];
     s.Tk0 = p.cu_tn ? p.cu_tn[b] : 0;
     s.off = p.cu_off[b];
-    const bool ok = s.sq >= 0 && s.sk >= 0 && s.nm == (s.sq + kTile - 1) / kTile && s.nn <= p.num_n &&
+    // the sequence must lie inside the packed arrays and agree with the metadata
+    const bool ok = s.q0 >= 0 && s.k0 >= 0 && s.sq >= 0 && s.sk >= 0 && s.q0 + s.sq <= p.rows_q &&
+                    s.k0 + s.sk <= p.rows_k && s.nm == (s.sq + kTile - 1) / kTile && s.nn <= p.num_n &&
                     s.off >= 0 && s.off + (long long)s.nm * s.nn <= p.total_n;
     s.bad = ok ? 0 : 1;
     if (!ok) s.nm = s.nn = 0;

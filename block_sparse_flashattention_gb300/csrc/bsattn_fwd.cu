@@ -19,6 +19,8 @@
 //               loads Q tiles and K/V tiles into rings of shared-memory stages
 //   warp 1      tcgen05 issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P in TMEM
 //   warp 2      owns the TMEM allocation
+//   warp 3      scheduler: claims work units and reads the head of their lists
+//               one unit ahead of the producer
 //   warps 4-7   softmax + O rescale + epilogue for tile 0 of the pair
 //   warps 8-11  the same for tile 1
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D);
@@ -125,7 +127,11 @@ struct Cfg {
 };
 
 
-__device__ __forceinline__ TileInfo tile_info(const FwdParams &p, int h, int T) {
+// Geometry of packed Q tile T of head h.  A varlen sequence whose offsets leave
+// the packed arrays (cu_q[b] < 0, cu_q[b + 1] past the packed query rows, or the
+// same for keys), or whose KV tiles outnumber the valid-length row stride, yields
+// no tile; then, when `err` is given, BSATTN_FLAG_BAD_SEQLENS is set.
+__device__ __forceinline__ TileInfo tile_info(const FwdParams &p, int h, int T, int32_t *err = nullptr) {
     TileInfo t;
     t.valid = 0;
     t.b = t.m = t.qrow0 = t.nvalid = t.krow0 = t.sk = t.nn = 0;
@@ -152,14 +158,23 @@ __device__ __forceinline__ TileInfo tile_info(const FwdParams &p, int h, int T) 
         }
         t.b = lo;
         t.m = T - p.cu_tm[lo];
-        sq = p.cu_q[lo + 1] - p.cu_q[lo];
-        t.sk = p.cu_k[lo + 1] - p.cu_k[lo];
-        t.qrow0 = p.cu_q[lo] + t.m * kTile;
-        t.krow0 = p.cu_k[lo];
+        // every load first (they go out together), then the checks
+        const int q0 = p.cu_q[lo], q1 = p.cu_q[lo + 1], k0 = p.cu_k[lo], k1 = p.cu_k[lo + 1];
+        const int off = p.cu_off[lo];
+        sq = q1 - q0;
+        t.sk = k1 - k0;
+        t.qrow0 = q0 + t.m * kTile;
+        t.krow0 = k0;
         t.nn = (t.sk + kTile - 1) / kTile;
         t.cnt_at = (long long)h * p.total_m + T;
-        t.idx_at = (long long)h * p.total_n + p.cu_off[lo] + (long long)t.m * t.nn;
-        if ((long long)p.cu_off[lo] + (long long)(t.m + 1) * t.nn > p.total_n) return t;
+        t.idx_at = (long long)h * p.total_n + off + (long long)t.m * t.nn;
+        const bool bad = q0 < 0 || q1 < q0 || q1 > p.seqlen_q || k0 < 0 || k1 < k0 || k1 > p.seqlen_k ||
+                         (p.vl && t.nn > p.vl_stride) || off < 0 ||
+                         (long long)off + (long long)(t.m + 1) * t.nn > p.total_n;
+        if (bad) {
+            if (err) atomicOr(err, BSATTN_FLAG_BAD_SEQLENS);
+            return t;
+        }
     }
     t.nvalid = sq - t.m * kTile;
     if (t.nvalid > kTile) t.nvalid = kTile;
@@ -219,9 +234,335 @@ __device__ __forceinline__ void cur_init(Cursor &c, const int32_t *ptr, int cnt,
     cur_advance(c, nn, err);
 }
 
+// Softmax, O rescale and epilogue of one tile slot t (warps 4-7: t = 0, 8-11:
+// t = 1).  Events come from the slot's S-ready barrier (bar_sr) with the item's
+// description in *sinfo_t; P is published in two halves (bar_pr, bar_pr + 8);
+// bar_ed acknowledges an end of unit.  The unit of each end-to-end run of events
+// is read from unit_ring_t (a unit is a pair of consecutive Q tiles).
+template <int D, bool kProxy, bool kPolled>
+__device__ __forceinline__ void softmax_role(const FwdParams &p, const uint32_t tmem, const int t,
+                                             const uint32_t warp, const uint32_t lane,
+                                             const uint32_t bar_sr, const uint32_t bar_pr,
+                                             const uint32_t bar_ed, const SInfo *sinfo_t,
+                                             const int32_t *unit_ring_t, uint8_t *epi,
+                                             volatile int *abort_flag) {
+    using C = Cfg<D>;
+    const uint32_t quarter = warp & 3u;
+    const int r = (int)(quarter * 32 + lane);                 // row of the tile
+    const uint32_t lane_addr = tmem + ((quarter * 32u) << 16);
+    const uint32_t s_col = (uint32_t)t * 128u;
+    const uint32_t o_col = 256u + (uint32_t)t * D;
+    const float sl2 = p.scale_log2;
+    uint32_t scount = 0, ucs = 0;
+    bool ok = true;
+    SInfo si;
+    // Next event (S tile, end of unit, or stop) for this tile.
+    auto wait_s = [&]() -> bool {
+        bool w = mbar_wait_lim<kPolled>(bar_sr, scount & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT, p.wait_limit);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) return false;
+        ++scount;
+        tc_fence_after();
+        const volatile SInfo *vs = sinfo_t;
+        si.n = vs->n;
+        si.flags = vs->flags;
+        si.lim = vs->lim;
+        return true;
+    };
+    while (ok) {
+        if (!(ok = wait_s())) break;
+        if (si.flags & kSStop) break;
+        // The producer wrote this unit's id before the events that led here.
+        const int u = *reinterpret_cast<const volatile int32_t *>(&unit_ring_t[ucs % kUnitRing]);
+        const int h = u / p.pairs_per_head;
+        const TileInfo ti = tile_info(p, h, 2 * (u - h * p.pairs_per_head) + t);
+        const int i_seq = ti.m * kTile + r;  // sequence-local query position
+        float m_run = -INFINITY, l_run = 0.f;
+        int j = 0;
+        while (true) {
+            if (si.flags & kSEnd) {
+                // Acknowledge the end of the unit: the MMA warp may signal again.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_ed);
+                break;
+            }
+            float s[128];
+            // Summary items: the sequence's last KV tile, if partial, counts with
+            // its true number of keys; its score column is read on its own (P
+            // overwrites the first half of the S columns).
+            const bool summary = kProxy && (si.flags & kSSummary) != 0;
+            int c_tail = -1;
+            if (summary && p.proxy_tail < kTile) {
+                const int ct = (p.num_n - 1) - si.n * kTile;
+                if (ct >= 0 && ct < kTile) c_tail = ct;
+            }
+            uint32_t s_tail_bits = 0u;
+            {
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(lane_addr + s_col + 0, v0);
+                tmem_ld32(lane_addr + s_col + 32, v1);
+                tmem_ld32(lane_addr + s_col + 64, v2);
+                tmem_ld32(lane_addr + s_col + 96, v3);
+                if (c_tail >= 0) tmem_ld1(lane_addr + s_col + (uint32_t)c_tail, s_tail_bits);
+                tmem_wait_ld();
+                reg_fence(v0);
+                reg_fence(v1);
+                reg_fence(v2);
+                reg_fence(v3);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    s[x] = __uint_as_float(v0[x]);
+                    s[32 + x] = __uint_as_float(v1[x]);
+                    s[64 + x] = __uint_as_float(v2[x]);
+                    s[96 + x] = __uint_as_float(v3[x]);
+                }
+            }
+            bool tail_kept = false;
+            if (si.flags & (kSMask | kSBound | (kProxy ? kSSummary : 0u))) {
+                // Keep-mask of the 128 columns as four 32-bit words; columns at or
+                // past si.lim (sequence end, valid length) are always dropped.
+                const int j0 = si.n * kTile;
+                const int lim = si.lim;
+                uint32_t keep[4];
+                if (summary) {
+                    // keep the summary columns whose tile is not computed exactly
+                    const uint32_t *sw = p.sel_words + ti.cnt_at * p.sel_words_per_row;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int wi = 4 * si.n + w;
+                        const uint32_t sel = wi < p.sel_words_per_row ? __ldg(sw + wi) : 0u;
+                        keep[w] = ~sel & span_bits(0, lim - 32 * w);
+                    }
+                    if (c_tail >= 0) {
+                        const uint32_t kw = (c_tail >> 5) == 0 ? keep[0]
+                                          : (c_tail >> 5) == 1 ? keep[1]
+                                          : (c_tail >> 5) == 2 ? keep[2] : keep[3];
+                        tail_kept = (kw >> (c_tail & 31)) & 1u;
+                    }
+                } else if (!(si.flags & kSMask) || p.kind == BSATTN_MASK_NONE) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) keep[w] = span_bits(0, lim - 32 * w);
+                } else if (p.kind == BSATTN_MASK_DOCUMENT) {
+                    const int32_t dq = __ldg(p.doc_q + ti.qrow0 + min(r, ti.nvalid - 1));
+                    const int32_t *dk = p.doc_k + (long long)ti.krow0 + j0;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t bits = 0;
+#pragma unroll 1
+                        for (int x = 0; x < 32; ++x) {
+                            const int c = 32 * w + x;
+                            if (c < lim && __ldg(dk + c) == dq) bits |= 1u << x;
+                        }
+                        keep[w] = bits;
+                    }
+                } else {
+                    const int diag = i_seq - j0 + 1;  // columns c < diag have j <= i
+                    int la = 0, ha = lim, hb = 0;
+                    if (p.kind == BSATTN_MASK_CAUSAL) {
+                        ha = min(lim, diag);
+                    } else if (p.kind == BSATTN_MASK_SLIDING_WINDOW) {
+                        la = diag <= p.window_left ? 0 : diag - p.window_left;
+                        ha = min(lim, diag);
+                        hb = min(ha, p.sink_tokens - j0);
+                    } else if (p.kind == BSATTN_MASK_PREFIX) {
+                        ha = min(lim, max(p.prefix_len - j0, diag));
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        keep[w] = span_bits(la - 32 * w, ha - 32 * w) | span_bits(0, hb - 32 * w);
+                }
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    if (keep[w] == 0xffffffffu) continue;
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        if (!((keep[w] >> x) & 1u)) s[32 * w + x] = -INFINITY;
+                }
+            }
+            float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+            float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+            for (int c = 12; c < 124; c += 8) {
+                mx0 = fmax3(mx0, s[c], s[c + 1]);
+                mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+            }
+            mx0 = fmax3(mx0, s[124], s[125]);
+            mx1 = fmax3(mx1, s[126], s[127]);
+            const float m_new = fmaxf(m_run, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
+            // Rescale O only when some row's running maximum grew by more than 2^8;
+            // otherwise keep the stale maximum (O / l at the end is the same).
+            const bool rescale = (j > 0) && __any_sync(0xffffffffu, (m_new - m_run) > 8.0f);
+            float alpha = 1.f;
+            if (j == 0 || rescale) {
+                if (rescale && m_new != -INFINITY) alpha = ex2_approx(m_run - m_new);
+                m_run = m_new;
+            }
+            const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
+            float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
+            auto p_half = [&](int c) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    float x0, x1;
+                    ffma2(x0, x1, s[c * 64 + 2 * x], s[c * 64 + 2 * x + 1], sl2, sl2, nm, nm);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    if (x & 1) fadd2(lb0, lb1, lb0, lb1, p0, p1);
+                    else fadd2(la0, la1, la0, la1, p0, p1);
+                    pk[x] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(lane_addr + s_col + c * 32, pk);
+            };
+            // Publish P to the MMA warp in two halves (keys 0-63, then 64-127).
+            auto publish = [&](int half) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_pr + 8u * (uint32_t)half);
+            };
+            p_half(0);
+            if (rescale) {
+                // S_t of this item was issued after the previous item's P.V, so
+                // its completion (observed above) means O_t is up to date.
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_addr + o_col + c * 32, v);
+                    tmem_wait_ld();
+                    reg_fence(v);
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
+                    tmem_st32(lane_addr + o_col + c * 32, v);
+                }
+            }
+            publish(0);
+            p_half(1);
+            publish(1);
+            const float l0 = la0 + lb0, l1 = la1 + lb1;
+            float l_item = l0 + l1;
+            if (summary) {
+                // a summary column stands for the 128 keys of its tile (the tail
+                // tile for proxy_tail keys)
+                l_item *= (float)kTile;
+                if (tail_kept) {
+                    const float pt = ex2_approx(fmaf(__uint_as_float(s_tail_bits), sl2, nm));
+                    l_item += (float)(p.proxy_tail - kTile) * pt;
+                }
+            }
+            l_run = l_run * alpha + l_item;
+            ++j;
+            if (!(ok = wait_s())) break;
+        }
+        if (!ok) break;
+        // Epilogue: O / l and LSE = ln(sum of exp(scale * s)).  Each lane holds one
+        // row of 128-byte blocks (64 columns in bf16, 32 in fp32).  A block goes
+        // through the warp's shared-memory scratch (16-byte pieces placed at
+        // piece ^ (row & 7), so that neither side conflicts on banks) and comes
+        // back with lane 8g + j holding piece j of rows 8g..8g+7: every store
+        // instruction then writes 4 whole 128-byte row segments.
+        const bool row_ok = ti.valid && r < ti.nvalid;
+        const bool empty = (j == 0) || !(l_run > 0.f);
+        const float inv = empty ? 0.f : 1.f / l_run;
+        const int gl = (int)(lane & 7u);
+        const int row0 = (int)(quarter * 32u) + 8 * (int)(lane >> 3);  // first row this lane stores
+        const int nrows = ti.valid ? min(max(ti.nvalid - row0, 0), 8) : 0;
+        // The lane number is re-read here (opaque to the compiler) so that the
+        // scratch addresses below are formed in the epilogue instead of being
+        // hoisted out of the unit loop and held in registers through it.
+        uint32_t ln;
+        asm volatile("mov.u32 %0, %%laneid;" : "=r"(ln));
+        uint4 *scr = reinterpret_cast<uint4 *>(epi + (warp - 4u) * 4096u);
+        // Writes this lane's block (row = lane) and reads back the 8 pieces it stores.
+        auto exchange = [&](uint32_t (&w)[32]) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                scr[ln * 8u + ((uint32_t)i ^ (ln & 7u))] =
+                    make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 x = scr[(ln >> 3) * 64u + (uint32_t)k * 8u + ((ln & 7u) ^ (uint32_t)k)];
+                w[4 * k] = x.x;
+                w[4 * k + 1] = x.y;
+                w[4 * k + 2] = x.z;
+                w[4 * k + 3] = x.w;
+            }
+            __syncwarp();
+        };
+        const long long row_step = (long long)p.H * D;             // elements between rows
+        const long long out0 = ((long long)(ti.qrow0 + row0) * p.H + h) * D;
+        if (p.out_f32) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t w[32];
+                if (j > 0) {
+                    tmem_ld32(lane_addr + o_col + c * 32, w);
+                    tmem_wait_ld();
+                    reg_fence(w);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) w[x] = 0u;
+                }
+#pragma unroll
+                for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(__uint_as_float(w[x]) * inv);
+                exchange(w);
+                float *dst = static_cast<float *>(p.out) + out0 + c * 32 + 4 * gl;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (k < nrows)
+                        *reinterpret_cast<uint4 *>(dst + k * row_step) =
+                            make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t w[32];
+                if (j > 0) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t v[32];
+                        tmem_ld32(lane_addr + o_col + c * 64 + hf * 32, v);
+                        tmem_wait_ld();
+                        reg_fence(v);
+#pragma unroll
+                        for (int x = 0; x < 16; ++x)
+                            w[16 * hf + x] = pack_bf16x2(__uint_as_float(v[2 * x]) * inv,
+                                                         __uint_as_float(v[2 * x + 1]) * inv);
+                    }
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) w[x] = 0u;
+                }
+                exchange(w);
+                uint16_t *dst = static_cast<uint16_t *>(p.out) + out0 + c * 64 + 8 * gl;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (k < nrows)
+                        *reinterpret_cast<uint4 *>(dst + k * row_step) =
+                            make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
+        }
+        if (row_ok) {
+            const float lse = empty ? -INFINITY : (m_run * 0.69314718055994530942f + logf(l_run));
+            const long long li = p.varlen
+                                     ? (long long)h * p.lse_row_stride + ti.qrow0 + r
+                                     : ((long long)ti.b * p.H + h) * p.lse_row_stride +
+                                           (long long)ti.m * kTile + r;
+            p.lse[li] = lse;
+        }
+        tc_fence_before();
+        ++ucs;
+    }
+}
+
 // kProxy: proxy-compensation build (summary items after each unit); the exact
-// build carries none of that code.
-template <int D, bool kProxy>
+// build carries none of that code.  kPolled: pipeline waits poll without
+// suspending and give up after p.wait_limit cycles (the build a lowered wait
+// limit runs; the waits of the default build use their fixed one-second limit).
+template <int D, bool kProxy, bool kPolled>
 __global__ void __launch_bounds__(kThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -293,8 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t un = 0;; ++un) {
                 // The next unit, prepared by the scheduler warp.
                 const uint32_t slot = un % kUnitDescs;
-                if (!mbar_wait(bar(C::bUF + slot), (un / kUnitDescs) & 1, abort_flag, p.err,
-                               BSATTN_FLAG_TIMEOUT))
+                if (!mbar_wait_lim<kPolled>(bar(C::bUF + slot), (un / kUnitDescs) & 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT, p.wait_limit))
                     goto producer_done;
                 const UnitDesc d = udesc[slot];
                 mbar_arrive_lead(lead, bar(C::bUE + slot));
@@ -304,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = u / p.pairs_per_head;
                 const TileInfo ti[2] = {d.ti[0], d.ti[1]};
                 for (int t = 0; t < 2; ++t) {
-                    if (!mbar_wait(bar(C::bQE + t), (uc & 1) ^ 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
+                    if (!mbar_wait_lim<kPolled>(bar(C::bQE + t), (uc & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT, p.wait_limit))
                         goto producer_done;
                     if (ti[t].valid) {
                         mbar_arrive_expect_tx_lead(lead, bar(C::bQF + t), C::kTileBytes);
@@ -379,8 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!kProxy && p0 && max(cm[0].head, cf[0].head) < 0) it.flags |= kLast0;
                     if (!kProxy && p1 && max(cm[1].head, cf[1].head) < 0) it.flags |= kLast1;
                     const uint32_t ks = kc % C::kStagesK;
-                    if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
+                    if (!mbar_wait_lim<kPolled>(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT, p.wait_limit))
                         goto producer_done;
                     if (p0) it.lim0 = min(min(kTile, ti[0].sk - c0 * kTile), vl0);
                     if (p1) it.lim1 = min(min(kTile, ti[1].sk - c1 * kTile), vl1);
@@ -392,9 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     x * 64, h, it.krow);
                     ++kc;
                     const uint32_t vs = vc % C::kStagesV;
-                    if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
+                    if (!mbar_wait_lim<kPolled>(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT, p.wait_limit)) {
+                        // V is not loaded: the K-stage barrier stops expecting its bytes,
+                        // so that the drain below sees the phase complete with K.
+                        mbar_complete_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
                         goto producer_done;
+                    }
                     for (int x = 0; x < C::kSub; ++x)
                         tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv, bar(C::bKF + ks),
                                     x * 64, h, it.krow);
@@ -421,8 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p0 && --sc0 < 0) it.flags |= kLast0;
                         if (p1 && --sc1 < 0) it.flags |= kLast1;
                         const uint32_t ks = kc % C::kStagesK;
-                        if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
-                                       BSATTN_FLAG_TIMEOUT))
+                        if (!mbar_wait_lim<kPolled>(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                       BSATTN_FLAG_TIMEOUT, p.wait_limit))
                             goto producer_done;
                         items[ks] = it;
                         mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), 2 * C::kTileBytes);
@@ -431,9 +776,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              bar(C::bKF + ks), x * 64, h, it.krow);
                         ++kc;
                         const uint32_t vs = vc % C::kStagesV;
-                        if (!mbar_wait(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
-                                       BSATTN_FLAG_TIMEOUT))
+                        if (!mbar_wait_lim<kPolled>(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag, p.err,
+                                       BSATTN_FLAG_TIMEOUT, p.wait_limit)) {
+                            mbar_complete_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
                             goto producer_done;
+                        }
                         for (int x = 0; x < C::kSub; ++x)
                             tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tvs,
                                              bar(C::bKF + ks), x * 64, h, it.krow);
@@ -442,8 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 {
                     const uint32_t ks = kc % C::kStagesK;
-                    if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
-                                   BSATTN_FLAG_TIMEOUT))
+                    if (!mbar_wait_lim<kPolled>(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                                   BSATTN_FLAG_TIMEOUT, p.wait_limit))
                         goto producer_done;
                     Item end;
                     end.krow = 0;
@@ -459,8 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             {
                 const uint32_t ks = kc % C::kStagesK;
-                if (!mbar_wait(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
-                               BSATTN_FLAG_TIMEOUT))
+                if (!mbar_wait_lim<kPolled>(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT, p.wait_limit))
                     goto producer_done;
                 Item stop;
                 stop.krow = 0;
@@ -519,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // then covers both (the common case when the MMA warp runs behind).
                 const bool both = mbar_test_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1);
                 if (!both &&
-                    !mbar_wait(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                    !mbar_wait_lim<kPolled>(bar(C::bPR + 2 * t), pc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT, p.wait_limit))
                     return false;
                 // The item's V tile landed before its K-stage wait completed.
                 const uint32_t vs = (uint32_t)pend[t] % C::kStagesV;
@@ -531,8 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kTile / 32; ++kk)
                     mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                            kk > 0 ? 1u : acc0);
-                if (!both && !mbar_wait(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
-                                        BSATTN_FLAG_TIMEOUT))
+                if (!both && !mbar_wait_lim<kPolled>(bar(C::bPR + 2 * t + 1), pc[t] & 1, abort_flag, p.err,
+                                        BSATTN_FLAG_TIMEOUT, p.wait_limit))
                     return false;
                 ++pc[t];
                 tc_fence_after();
@@ -549,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // otherwise complete two phases before the softmax waits on it.
             auto signal_s = [&](int t, int32_t n, int32_t lim, uint32_t fl) -> bool {
                 if (need_ed[t]) {
-                    if (!mbar_wait(bar(C::bED + t), edc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))
+                    if (!mbar_wait_lim<kPolled>(bar(C::bED + t), edc[t] & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT, p.wait_limit))
                         return false;
                     ++edc[t];
                     need_ed[t] = false;
@@ -563,8 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             while (ok) {
                 const uint32_t ks = kc % C::kStagesK;
-                if (!(ok = mbar_wait(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
-                                     BSATTN_FLAG_TIMEOUT)))
+                if (!(ok = mbar_wait_lim<kPolled>(bar(C::bKF + ks), (kc / C::kStagesK) & 1, abort_flag, p.err,
+                                     BSATTN_FLAG_TIMEOUT, p.wait_limit)))
                     break;
                 Item it;
                 {
@@ -591,8 +938,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
                         if (ok && !have_q[t])
-                            ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
-                                           BSATTN_FLAG_TIMEOUT);
+                            ok = mbar_wait_lim<kPolled>(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                           BSATTN_FLAG_TIMEOUT, p.wait_limit);
                     if (!ok) break;
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
@@ -620,8 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(it.flags & (t ? kPart1 : kPart0))) continue;
                     if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
                     if (!have_q[t]) {
-                        if (!(ok = mbar_wait(bar(C::bQF + t), uc & 1, abort_flag, p.err,
-                                             BSATTN_FLAG_TIMEOUT)))
+                        if (!(ok = mbar_wait_lim<kPolled>(bar(C::bQF + t), uc & 1, abort_flag, p.err,
+                                             BSATTN_FLAG_TIMEOUT, p.wait_limit)))
                             break;
                         have_q[t] = true;
                         tc_fence_after();
@@ -684,8 +1031,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (uint32_t n = 0;; ++n) {
                 const uint32_t slot = n % kUnitDescs;
-                if (!mbar_wait(bar(C::bUE + slot), ((n / kUnitDescs) & 1) ^ 1, abort_flag, p.err,
-                               BSATTN_FLAG_TIMEOUT))
+                if (!mbar_wait_lim<kPolled>(bar(C::bUE + slot), ((n / kUnitDescs) & 1) ^ 1, abort_flag, p.err,
+                               BSATTN_FLAG_TIMEOUT, p.wait_limit))
                     break;
                 UnitDesc &d = udesc[slot];
                 d.u = u;
@@ -698,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pr = u - h * p.pairs_per_head;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    const TileInfo ti = tile_info(p, h, 2 * pr + t);
+                    const TileInfo ti = tile_info(p, h, 2 * pr + t, lead ? p.err : nullptr);
                     d.ti[t] = ti;
                     int cm = 0, cf = 0, m0 = -1, m1 = -1, f0 = -1, f1 = -1, vl = kTile;
                     if (ti.valid) {
@@ -734,316 +1081,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- softmax --
         regs_claim<kSoftmaxRegs>();
         const int t = (warp >= 8) ? 1 : 0;
-        const uint32_t quarter = warp & 3u;
-        const int r = (int)(quarter * 32 + lane);                 // row of the tile
-        const uint32_t lane_addr = tmem + ((quarter * 32u) << 16);
-        const uint32_t s_col = (uint32_t)t * 128u;
-        const uint32_t o_col = 256u + (uint32_t)t * D;
-        const float sl2 = p.scale_log2;
-        uint32_t scount = 0, ucs = 0;
-        bool ok = true;
-        SInfo si;
-        // Next event (S tile, end of unit, or stop) for this tile.
-        auto wait_s = [&]() -> bool {
-            bool w = mbar_wait(bar(C::bSR + t), scount & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-            w = __all_sync(0xffffffffu, w);
-            if (!w) return false;
-            ++scount;
-            tc_fence_after();
-            const volatile SInfo *vs = &sinfo[t];
-            si.n = vs->n;
-            si.flags = vs->flags;
-            si.lim = vs->lim;
-            return true;
-        };
-        while (ok) {
-            if (!(ok = wait_s())) break;
-            if (si.flags & kSStop) break;
-            // The producer wrote this unit's id before the events that led here.
-            const int u = *reinterpret_cast<const volatile int32_t *>(&unit_ring[ucs % kUnitRing]);
-            const int h = u / p.pairs_per_head;
-            const int pr = u - h * p.pairs_per_head;
-            const TileInfo ti = tile_info(p, h, 2 * pr + t);
-            const int i_seq = ti.m * kTile + r;  // sequence-local query position
-            float m_run = -INFINITY, l_run = 0.f;
-            int j = 0;
-            while (true) {
-                if (si.flags & kSEnd) {
-                    // Acknowledge the end of the unit: the MMA warp may signal again.
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::bED + t));
-                    break;
-                }
-                float s[128];
-                // Summary items: the sequence's last KV tile, if partial, counts with
-                // its true number of keys; its score column is read on its own (P
-                // overwrites the first half of the S columns).
-                const bool summary = kProxy && (si.flags & kSSummary) != 0;
-                int c_tail = -1;
-                if (summary && p.proxy_tail < kTile) {
-                    const int ct = (p.num_n - 1) - si.n * kTile;
-                    if (ct >= 0 && ct < kTile) c_tail = ct;
-                }
-                uint32_t s_tail_bits = 0u;
-                {
-                    uint32_t v0[32], v1[32], v2[32], v3[32];
-                    tmem_ld32(lane_addr + s_col + 0, v0);
-                    tmem_ld32(lane_addr + s_col + 32, v1);
-                    tmem_ld32(lane_addr + s_col + 64, v2);
-                    tmem_ld32(lane_addr + s_col + 96, v3);
-                    if (c_tail >= 0) tmem_ld1(lane_addr + s_col + (uint32_t)c_tail, s_tail_bits);
-                    tmem_wait_ld();
-                    reg_fence(v0);
-                    reg_fence(v1);
-                    reg_fence(v2);
-                    reg_fence(v3);
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        s[x] = __uint_as_float(v0[x]);
-                        s[32 + x] = __uint_as_float(v1[x]);
-                        s[64 + x] = __uint_as_float(v2[x]);
-                        s[96 + x] = __uint_as_float(v3[x]);
-                    }
-                }
-                bool tail_kept = false;
-                if (si.flags & (kSMask | kSBound | (kProxy ? kSSummary : 0u))) {
-                    // Keep-mask of the 128 columns as four 32-bit words; columns at or
-                    // past si.lim (sequence end, valid length) are always dropped.
-                    const int j0 = si.n * kTile;
-                    const int lim = si.lim;
-                    uint32_t keep[4];
-                    if (summary) {
-                        // keep the summary columns whose tile is not computed exactly
-                        const uint32_t *sw = p.sel_words + ti.cnt_at * p.sel_words_per_row;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int wi = 4 * si.n + w;
-                            const uint32_t sel = wi < p.sel_words_per_row ? __ldg(sw + wi) : 0u;
-                            keep[w] = ~sel & span_bits(0, lim - 32 * w);
-                        }
-                        if (c_tail >= 0) {
-                            const uint32_t kw = (c_tail >> 5) == 0 ? keep[0]
-                                              : (c_tail >> 5) == 1 ? keep[1]
-                                              : (c_tail >> 5) == 2 ? keep[2] : keep[3];
-                            tail_kept = (kw >> (c_tail & 31)) & 1u;
-                        }
-                    } else if (!(si.flags & kSMask) || p.kind == BSATTN_MASK_NONE) {
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) keep[w] = span_bits(0, lim - 32 * w);
-                    } else if (p.kind == BSATTN_MASK_DOCUMENT) {
-                        const int32_t dq = __ldg(p.doc_q + ti.qrow0 + min(r, ti.nvalid - 1));
-                        const int32_t *dk = p.doc_k + (long long)ti.krow0 + j0;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint32_t bits = 0;
-#pragma unroll 1
-                            for (int x = 0; x < 32; ++x) {
-                                const int c = 32 * w + x;
-                                if (c < lim && __ldg(dk + c) == dq) bits |= 1u << x;
-                            }
-                            keep[w] = bits;
-                        }
-                    } else {
-                        const int diag = i_seq - j0 + 1;  // columns c < diag have j <= i
-                        int la = 0, ha = lim, hb = 0;
-                        if (p.kind == BSATTN_MASK_CAUSAL) {
-                            ha = min(lim, diag);
-                        } else if (p.kind == BSATTN_MASK_SLIDING_WINDOW) {
-                            la = diag <= p.window_left ? 0 : diag - p.window_left;
-                            ha = min(lim, diag);
-                            hb = min(ha, p.sink_tokens - j0);
-                        } else if (p.kind == BSATTN_MASK_PREFIX) {
-                            ha = min(lim, max(p.prefix_len - j0, diag));
-                        }
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            keep[w] = span_bits(la - 32 * w, ha - 32 * w) | span_bits(0, hb - 32 * w);
-                    }
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        if (keep[w] == 0xffffffffu) continue;
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            if (!((keep[w] >> x) & 1u)) s[32 * w + x] = -INFINITY;
-                    }
-                }
-                float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-                float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-                for (int c = 12; c < 124; c += 8) {
-                    mx0 = fmax3(mx0, s[c], s[c + 1]);
-                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-                }
-                mx0 = fmax3(mx0, s[124], s[125]);
-                mx1 = fmax3(mx1, s[126], s[127]);
-                const float m_new = fmaxf(m_run, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
-                // Rescale O only when some row's running maximum grew by more than 2^8;
-                // otherwise keep the stale maximum (O / l at the end is the same).
-                const bool rescale = (j > 0) && __any_sync(0xffffffffu, (m_new - m_run) > 8.0f);
-                float alpha = 1.f;
-                if (j == 0 || rescale) {
-                    if (rescale && m_new != -INFINITY) alpha = ex2_approx(m_run - m_new);
-                    m_run = m_new;
-                }
-                const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
-                float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
-                auto p_half = [&](int c) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        float x0, x1;
-                        ffma2(x0, x1, s[c * 64 + 2 * x], s[c * 64 + 2 * x + 1], sl2, sl2, nm, nm);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
-                        if (x & 1) fadd2(lb0, lb1, lb0, lb1, p0, p1);
-                        else fadd2(la0, la1, la0, la1, p0, p1);
-                        pk[x] = pack_bf16x2(p0, p1);
-                    }
-                    tmem_st32(lane_addr + s_col + c * 32, pk);
-                };
-                // Publish P to the MMA warp in two halves (keys 0-63, then 64-127).
-                auto publish = [&](int half) {
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::bPR + 2 * t + half));
-                };
-                p_half(0);
-                if (rescale) {
-                    // S_t of this item was issued after the previous item's P.V, so
-                    // its completion (observed above) means O_t is up to date.
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(lane_addr + o_col + c * 32, v);
-                        tmem_wait_ld();
-                        reg_fence(v);
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
-                        tmem_st32(lane_addr + o_col + c * 32, v);
-                    }
-                }
-                publish(0);
-                p_half(1);
-                publish(1);
-                const float l0 = la0 + lb0, l1 = la1 + lb1;
-                float l_item = l0 + l1;
-                if (summary) {
-                    // a summary column stands for the 128 keys of its tile (the tail
-                    // tile for proxy_tail keys)
-                    l_item *= (float)kTile;
-                    if (tail_kept) {
-                        const float pt = ex2_approx(fmaf(__uint_as_float(s_tail_bits), sl2, nm));
-                        l_item += (float)(p.proxy_tail - kTile) * pt;
-                    }
-                }
-                l_run = l_run * alpha + l_item;
-                ++j;
-                if (!(ok = wait_s())) break;
-            }
-            if (!ok) break;
-            // Epilogue: O / l and LSE = ln(sum of exp(scale * s)).  Each lane holds one
-            // row of 128-byte blocks (64 columns in bf16, 32 in fp32).  A block goes
-            // through the warp's shared-memory scratch (16-byte pieces placed at
-            // piece ^ (row & 7), so that neither side conflicts on banks) and comes
-            // back with lane 8g + j holding piece j of rows 8g..8g+7: every store
-            // instruction then writes 4 whole 128-byte row segments.
-            const bool row_ok = ti.valid && r < ti.nvalid;
-            const bool empty = (j == 0) || !(l_run > 0.f);
-            const float inv = empty ? 0.f : 1.f / l_run;
-            const int gl = (int)(lane & 7u);
-            const int row0 = (int)(quarter * 32u) + 8 * (int)(lane >> 3);  // first row this lane stores
-            const int nrows = ti.valid ? min(max(ti.nvalid - row0, 0), 8) : 0;
-            // The lane number is re-read here (opaque to the compiler) so that the
-            // scratch addresses below are formed in the epilogue instead of being
-            // hoisted out of the unit loop and held in registers through it.
-            uint32_t ln;
-            asm volatile("mov.u32 %0, %%laneid;" : "=r"(ln));
-            uint4 *scr = reinterpret_cast<uint4 *>(gbase + C::kEpi + (warp - 4u) * 4096u);
-            // Writes this lane's block (row = lane) and reads back the 8 pieces it stores.
-            auto exchange = [&](uint32_t (&w)[32]) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    scr[ln * 8u + ((uint32_t)i ^ (ln & 7u))] =
-                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 x = scr[(ln >> 3) * 64u + (uint32_t)k * 8u + ((ln & 7u) ^ (uint32_t)k)];
-                    w[4 * k] = x.x;
-                    w[4 * k + 1] = x.y;
-                    w[4 * k + 2] = x.z;
-                    w[4 * k + 3] = x.w;
-                }
-                __syncwarp();
-            };
-            const long long row_step = (long long)p.H * D;             // elements between rows
-            const long long out0 = ((long long)(ti.qrow0 + row0) * p.H + h) * D;
-            if (p.out_f32) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t w[32];
-                    if (j > 0) {
-                        tmem_ld32(lane_addr + o_col + c * 32, w);
-                        tmem_wait_ld();
-                        reg_fence(w);
-                    } else {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) w[x] = 0u;
-                    }
-#pragma unroll
-                    for (int x = 0; x < 32; ++x) w[x] = __float_as_uint(__uint_as_float(w[x]) * inv);
-                    exchange(w);
-                    float *dst = static_cast<float *>(p.out) + out0 + c * 32 + 4 * gl;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        if (k < nrows)
-                            *reinterpret_cast<uint4 *>(dst + k * row_step) =
-                                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t w[32];
-                    if (j > 0) {
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t v[32];
-                            tmem_ld32(lane_addr + o_col + c * 64 + hf * 32, v);
-                            tmem_wait_ld();
-                            reg_fence(v);
-#pragma unroll
-                            for (int x = 0; x < 16; ++x)
-                                w[16 * hf + x] = pack_bf16x2(__uint_as_float(v[2 * x]) * inv,
-                                                             __uint_as_float(v[2 * x + 1]) * inv);
-                        }
-                    } else {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) w[x] = 0u;
-                    }
-                    exchange(w);
-                    uint16_t *dst = static_cast<uint16_t *>(p.out) + out0 + c * 64 + 8 * gl;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        if (k < nrows)
-                            *reinterpret_cast<uint4 *>(dst + k * row_step) =
-                                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-                }
-            }
-            if (row_ok) {
-                const float lse = empty ? -INFINITY : (m_run * 0.69314718055994530942f + logf(l_run));
-                const long long li = p.varlen
-                                         ? (long long)h * p.lse_row_stride + ti.qrow0 + r
-                                         : ((long long)ti.b * p.H + h) * p.lse_row_stride +
-                                               (long long)ti.m * kTile + r;
-                p.lse[li] = lse;
-            }
-            tc_fence_before();
-            ++ucs;
-        }
+        softmax_role<D, kProxy, kPolled>(p, tmem, t, warp, lane, bar(C::bSR + t), bar(C::bPR + 2 * t),
+                                                bar(C::bED + t), &sinfo[t], unit_ring, gbase + C::kEpi,
+                                                abort_flag);
     }
 
     tc_fence_before();
@@ -1116,7 +1156,7 @@ __global__ void __launch_bounds__(1024, 1) bsattn_schedule_kernel(const __grid_c
     }
 }
 
-template <int D, bool kProxy>
+template <int D, bool kProxy, bool kPolled>
 cudaError_t prepare_fwd_kernel() {
     using C = Cfg<D>;
     static int attr_set_for_device[64] = {0};
@@ -1128,25 +1168,34 @@ cudaError_t prepare_fwd_kernel() {
         // The register split inside the kernel assumes exactly kLaunchRegs per
         // thread at launch; refuse to run a build where that does not hold.
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D, kProxy>);
+        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D, kProxy, kPolled>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, kProxy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmemAlloc);
+        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, kProxy, kPolled>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
     }
     return cudaSuccess;
 }
 
+template <int D, bool kProxy, bool kPolled>
+cudaError_t launch_fwd_kernel(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs,
+                              int grid, cudaStream_t stream) {
+    cudaError_t e = prepare_fwd_kernel<D, kProxy, kPolled>();
+    if (e != cudaSuccess) return e;
+    bsattn_fwd_kernel<D, kProxy, kPolled><<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(p, tq, tk, tv, tks,
+                                                                                          tvs);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                          const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs,
                          int num_sms, cudaStream_t stream) {
-    using C = Cfg<D>;
-    cudaError_t e = p.proxy ? prepare_fwd_kernel<D, true>() : prepare_fwd_kernel<D, false>();
-    if (e != cudaSuccess) return e;
     if (p.num_units <= 0) return cudaSuccess;
+    cudaError_t e;
     if (p.dynamic) {
         const size_t key_bytes = (size_t)p.num_units * sizeof(uint16_t);
         if (key_bytes > 48 * 1024) {
@@ -1159,11 +1208,12 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
         if (e != cudaSuccess) return e;
     }
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-    if (p.proxy)
-        bsattn_fwd_kernel<D, true><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
-    else
-        bsattn_fwd_kernel<D, false><<<grid, kThreads, C::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
-    return cudaGetLastError();
+    // A wait limit below the default (a test lowering it) runs the build whose
+    // waits poll against that limit; the proxy build keeps its fixed limit.
+    if (p.proxy) return launch_fwd_kernel<D, true, false>(p, tq, tk, tv, tks, tvs, grid, stream);
+    if (p.wait_limit < kDefaultWaitLimitCycles)
+        return launch_fwd_kernel<D, false, true>(p, tq, tk, tv, tks, tvs, grid, stream);
+    return launch_fwd_kernel<D, false, false>(p, tq, tk, tv, tks, tvs, grid, stream);
 }
 
 }  // namespace

@@ -78,7 +78,12 @@ struct FwdParams {
     int proxy_tail;
     uint32_t *sched_counter;       // workspace: next slot of sched_order
     int32_t *sched_order;          // workspace: units, heaviest first
+    long long wait_limit;          // cycles after which a pipeline wait gives up
 };
+
+// Cycles after which a forward pipeline wait gives up unless a test lowers it
+// (about one second at 2 GHz).
+constexpr long long kDefaultWaitLimitCycles = 1ll << 31;
 
 // Units the scheduling pass can order (its per-unit keys live in shared memory).
 constexpr int kMaxScheduledUnits = 98304;

@@ -183,6 +183,17 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
         m = T - p.cu_tm[lo];
         const long long sq = (long long)p.cu_q[lo + 1] - p.cu_q[lo];
         g.sk = (long long)p.cu_k[lo + 1] - p.cu_k[lo];
+        // A sequence outside the packed arrays (when their row counts are given),
+        // with negative offsets, or with more KV tiles than the valid-length row
+        // stride has no rows here.
+        const bool outside = p.cu_q[lo] < 0 || p.cu_k[lo] < 0 || sq < 0 || g.sk < 0 ||
+                             (p.seqlen_q > 0 && p.cu_q[lo + 1] > p.seqlen_q) ||
+                             (p.seqlen_k > 0 && p.cu_k[lo + 1] > p.seqlen_k) ||
+                             (p.vl && cdiv_ll(g.sk, kTile) > p.vl_stride);
+        if (outside) {
+            if (lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_SEQLENS);
+            return;
+        }
         g.i_min = (long long)m * kTile;
         g.i_max = (g.i_min + kTile < sq ? g.i_min + kTile : sq) - 1;
         g.qbase = p.cu_q[lo];
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
         nn = (int)cdiv_ll(g.sk, kTile);
         cnt_at = (long long)h * p.total_m + T;
         idx_at = (long long)h * p.total_n + p.cu_off[lo] + (long long)m * nn;
-        if ((long long)p.cu_off[lo] + (long long)(m + 1) * nn > p.total_n) {
+        if (p.cu_off[lo] < 0 || (long long)p.cu_off[lo] + (long long)(m + 1) * nn > p.total_n) {
             if (lane == 0 && p.err) atomicOr(p.err, BSATTN_FLAG_BAD_SEQLENS);
             return;
         }

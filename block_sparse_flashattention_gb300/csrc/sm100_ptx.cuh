@@ -89,6 +89,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// The same with a limit given at run time, polling with non-blocking tests:
+// a try_wait may suspend the thread until the phase completes, which would hide
+// a short limit.  kPolled = false is the plain wait above (the limit is then
+// kWaitLimitCycles).
+template <bool kPolled>
+__device__ __forceinline__ bool mbar_wait_lim(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              int *err, int flag_bit, long long limit) {
+    if constexpr (!kPolled) {
+        return mbar_wait(bar, parity, abort, err, flag_bit);
+    } else {
+        const long long t0 = clock64();
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (*abort) return false;
+            if (clock64() - t0 > limit) {
+                *abort = 1;
+                if (err) atomicOr(err, flag_bit);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait used while tearing down after an abort: ignores the abort flag.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -96,6 +119,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     while (clock64() - t0 < kWaitLimitCycles)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// Counts `bytes` of the current phase's expected transaction bytes as arrived
+// without a copy (used to cancel a load that an aborting producer did not issue).
+__device__ __forceinline__ void mbar_complete_tx_lead(uint32_t lead, uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n\t}" ::"r"(bar),
+        "r"(bytes), "r"(lead)
+        : "memory");
 }
 
 // ------------------------------------------------------- register split --

@@ -74,7 +74,7 @@ typedef enum {
 #define BSATTN_FLAG_BAD_COUNT 0x1   /* a block count outside [0, num_n(b)] was clamped        */
 #define BSATTN_FLAG_BAD_INDEX 0x2   /* a block index outside [0, num_n(b)) was skipped        */
 #define BSATTN_FLAG_TIMEOUT 0x4     /* a pipeline wait exceeded its limit; the CTA stopped   */
-#define BSATTN_FLAG_BAD_SEQLENS 0x8 /* cu_seqlens disagree with the sizes given in the meta  */
+#define BSATTN_FLAG_BAD_SEQLENS 0x8 /* cu_seqlens disagree with the meta or leave the packed rows */
 
 typedef struct {
     int32_t window_left;      /* SLIDING_WINDOW: keys with 0 <= i - j < window_left      */
@@ -125,7 +125,10 @@ typedef struct {
  * cu_seqlens_q  varlen: device int32 [B+1] packed row offsets; batched: NULL.
  * cu_seqlens_k  likewise for keys.
  * seqlen_q/_k   batched: per-sequence lengths (num_m == ceil(seqlen_q/128),
- *               num_n == ceil(seqlen_k/128) is checked); varlen: ignored.
+ *               num_n == ceil(seqlen_k/128) is checked); varlen: the packed row
+ *               counts of q and k, or 0.  When positive, a sequence whose offsets
+ *               reach past them (or are negative) is rejected: its rows are not
+ *               written and BSATTN_FLAG_BAD_SEQLENS is set.
  * kv_valid_len  optional device int32 [B, meta->num_n]: valid keys at the start
  *               of each KV tile (the rest of the tile is masked on mask blocks).
  * kind, mp      mask_mod (mp may be NULL unless the kind needs it).
@@ -257,7 +260,11 @@ bsattn_status bsattn_build_meta_bsr(const int32_t *block_indptr, const int32_t *
  *               (seqlen_q = total packed rows); contiguous, 16-byte aligned.
  * k, v          device bf16, same layout with seqlen_k.
  * B, H, D       D in {64, 128}; H equal for q and k/v.
- * cu_seqlens_*  varlen: device int32 [B+1]; batched: NULL.
+ * cu_seqlens_*  varlen: device int32 [B+1]; batched: NULL.  A sequence whose
+ *               offsets are negative, decrease, or reach past seqlen_q / seqlen_k
+ *               (the packed row counts), or that has more KV tiles than
+ *               meta->num_n while kv_valid_len is given, is skipped: none of its
+ *               out / lse rows is written and BSATTN_FLAG_BAD_SEQLENS is set.
  * meta          lists as written by bsattn_build_meta (or the caller, same format;
  *               indices out of range are skipped and flagged).
  * kv_valid_len, kind, mp   as for bsattn_build_meta (applied on mask-list tiles).
@@ -337,7 +344,10 @@ bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
  * BSATTN_ERR_CAPACITY before any CUDA call (use bsattn_fwd with a workspace).
  * Setup: the first call on each device resolves the scratch array's device
  * address (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  Zeroing: the claim counter in the scratch is
+ * call before any stream capture.  The address is kept per CUDA context: after
+ * cudaDeviceReset (or any re-creation of the device's primary context) the next
+ * call resolves it again, so that first call after a reset also belongs before
+ * any capture.  Zeroing: the claim counter in the scratch is
  * reset on the stream by the scheduling pass of every call.
  * Concurrency: all calls on one device share the one scratch array, so calls
  * that may overlap (different streams, or threads without ordering) race on it
@@ -383,7 +393,8 @@ bsattn_status bsattn_fwd_static_scratch(const void *q, const void *k, const void
  *               entry lies outside [0, num_n(b)) (skipped), a count outside
  *               [0, num_n(b)] (clamped) or a row lists a tile twice;
  *               BSATTN_FLAG_BAD_SEQLENS when a varlen sequence's offsets disagree
- *               with the metadata (its rows are not written);
+ *               with the metadata or reach past the packed rows (its rows are not
+ *               written);
  *               BSATTN_FLAG_TIMEOUT as for bsattn_fwd.
  * D other than 64 or 128 -> BSATTN_ERR_UNSUPPORTED.
  * Asynchronous on `stream`; the arrays must stay valid until it completes.
@@ -406,6 +417,22 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
  * tile and head); each of the nine regions rounded up to 256 bytes.
  */
 bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
+
+/*
+ * bsattn_testing_set_wait_limit -- testing hook, not for production use; the
+ * pages have no counterpart.  Sets the number of SM clock cycles after which a
+ * pipeline wait (an mbarrier wait between the roles of a CTA) of later
+ * bsattn_fwd and bsattn_fwd_static_scratch launches from this process gives up.
+ * A limit below the default runs a build of the same kernel whose waits poll
+ * without suspending the thread (a suspended wait could outlast a short limit);
+ * the default build is used otherwise.  A CTA whose wait gives up sets
+ * BSATTN_FLAG_TIMEOUT in err_flag, waits for the copies and tensor-core products
+ * it has already issued, frees its tensor memory and exits; out / lse are then
+ * incomplete.  cycles <= 0 restores the default of 2^31 cycles (about one
+ * second at 2 GHz).  bsattn_fwd_proxy keeps the default.  The setting is
+ * process-wide and read when a call is made; always BSATTN_OK.
+ */
+bsattn_status bsattn_testing_set_wait_limit(long long cycles);
 
 /* Human-readable name of a status code (static string). */
 const char *bsattn_status_string(bsattn_status status);

@@ -11,7 +11,7 @@ torch = pytest.importorskip("torch")
 
 import block_sparse_flashattention_gb300 as bsa  # noqa: E402
 import oracle  # noqa: E402
-from tests.gpu_run import DeviceWorkload, meta_to_numpy  # noqa: E402
+from workloads.device import DeviceWorkload, meta_to_numpy  # noqa: E402
 from workloads import make_workload  # noqa: E402
 from workloads.configs import (MASK_CAUSAL, MASK_NONE, MASK_PREFIX,  # noqa: E402
                                MASK_SLIDING_WINDOW, Workload)

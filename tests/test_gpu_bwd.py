@@ -17,7 +17,7 @@ torch = pytest.importorskip("torch")
 
 import block_sparse_flashattention_gb300 as bsa  # noqa: E402
 import oracle  # noqa: E402
-from tests.gpu_run import DeviceWorkload, bf16_to_device  # noqa: E402
+from workloads.device import DeviceWorkload, bf16_to_device  # noqa: E402
 from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX,  # noqa: E402
                                MASK_SLIDING_WINDOW, random_workload)
 

@@ -9,7 +9,7 @@ torch = pytest.importorskip("torch")
 import block_sparse_flashattention_gb300 as bsa  # noqa: E402
 import oracle  # noqa: E402
 from workloads.formats import to_bitmask, to_bsr  # noqa: E402
-from tests.gpu_run import DeviceWorkload, meta_to_numpy  # noqa: E402
+from workloads.device import DeviceWorkload, meta_to_numpy  # noqa: E402
 from workloads import make_workload  # noqa: E402
 from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE,  # noqa: E402
                                MASK_SLIDING_WINDOW, random_workload)

@@ -5,16 +5,17 @@ the kernel's fp32 output; the bf16 output is checked to be exactly the
 round-to-nearest-even of that fp32 output (a bf16 result cannot meet an
 absolute 5e-3 bar on its own once |O| >= 2, where half a bf16 ulp is 0.0078).
 
-Small configs are compared element by element; the two full-size configs at
-sampled (row, head) outputs the oracle computes one by one, in the same launch
-configuration the benchmark times, plus properties that hold at any size."""
+Small configs are compared element by element; the two full-size configs on
+every row of their first and last head and at sampled (row, head) outputs of
+the rest, in the same launch configuration the benchmark times, plus properties
+that hold at any size."""
 import numpy as np
 import pytest
 import torch
 
 import block_sparse_flashattention_gb300 as bsa
 import oracle
-from tests.gpu_run import DeviceWorkload, meta_from_numpy
+from workloads.device import DeviceWorkload, meta_from_numpy
 from workloads import bf16_bits_to_f32, make_workload
 from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX,
                                MASK_SLIDING_WINDOW, random_workload)
@@ -203,16 +204,22 @@ def _sample_rows(wl, n_tiles, seed):
 
 
 @pytest.mark.parametrize("cfg", [4, 5])
-def test_fwd_full_size_sampled(cfg):
+def test_fwd_full_size_whole_heads_and_samples(cfg):
+    """Every output row of the first and the last head, element by element, plus
+    sampled rows of randomly chosen tiles and heads across the rest."""
     wl = make_workload(cfg)
     (q, k, v), got_o, got_l = _run(wl)
     ref_meta = oracle.build_meta(wl)
+    S = int(wl.seqlens_q[0])
+    g_o_all = got_o.reshape(S, wl.H, wl.D)
+    g_l_all = got_l.reshape(wl.H, S)
+    for h in (0, wl.H - 1):
+        tok = np.arange(S, dtype=np.int32)
+        ref_o, ref_l = oracle.fwd_rows(wl, q, k, v, ref_meta, tok, np.full(S, h, np.int32))
+        _compare(g_o_all[:, h], g_l_all[h], ref_o, ref_l)
     tok, head = _sample_rows(wl, 48, seed=cfg)
     ref_o, ref_l = oracle.fwd_rows(wl, q, k, v, ref_meta, tok, head)
-    S = int(wl.seqlens_q[0])
-    g_o = got_o.reshape(S, wl.H, wl.D)[tok, head]
-    g_l = got_l.reshape(wl.H, S)[head, tok]
-    _compare(g_o, g_l, ref_o, ref_l)
+    _compare(g_o_all[tok, head], g_l_all[head, tok], ref_o, ref_l)
     # properties at every output: finite, no empty rows in these configs, and each
     # O row a convex combination of V rows (bounded by the largest |v|)
     assert np.all(np.isfinite(got_l))

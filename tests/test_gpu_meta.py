@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from tests.gpu_run import DeviceWorkload, meta_to_numpy
+from workloads.device import DeviceWorkload, meta_to_numpy
 from workloads import make_workload
 from workloads.configs import (MASK_CAUSAL, MASK_DOCUMENT, MASK_NONE, MASK_PREFIX,
                                MASK_SLIDING_WINDOW, random_workload)
@@ -72,7 +72,7 @@ def test_meta_error_flag_on_inconsistent_varlen_totals():
     wl = random_workload(120, B=2, H=2, D=64, seqlens_q=[300, 200], varlen=True, kind=MASK_CAUSAL)
     dev = torch.device("cuda")
     import block_sparse_flashattention_gb300 as bsa
-    from tests.gpu_run import i32
+    from workloads.device import i32
     small_m, small_n = wl.total_m_blocks - 1, wl.total_n_blocks - 3
     meta = bsa.alloc_meta(wl.B, wl.H, varlen=True, total_m_blocks=small_m, total_n_blocks=small_n,
                           max_num_n=wl.num_n, device=dev)

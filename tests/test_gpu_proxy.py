@@ -12,7 +12,7 @@ torch = pytest.importorskip("torch")
 
 import block_sparse_flashattention_gb300 as bsa  # noqa: E402
 import oracle  # noqa: E402
-from tests.gpu_run import DeviceWorkload  # noqa: E402
+from workloads.device import DeviceWorkload  # noqa: E402
 from workloads.configs import MASK_NONE, random_workload  # noqa: E402
 from workloads.formats import to_bitmask  # noqa: E402
 

@@ -1,7 +1,8 @@
 """Moves a seeded workload to the GPU and runs the library on it (harness code).
 
 Used by the GPU tests, __graft_entry__.smoke() and bench.py.  It only uploads
-inputs and calls the public API of block_sparse_flashattention_gb300.
+inputs, calls the public API of block_sparse_flashattention_gb300 and copies
+results back; it holds none of the method's arithmetic.
 """
 from __future__ import annotations
 
