@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--no-meta-formats", action="store_true",
                     help="skip the side measurements (metadata formats, proxy A/B)")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward timing")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the forward timing of configs 3 and 5")
+    ap.add_argument("--no-oracle-timing", action="store_true",
+                    help="skip the oracle timing over configs 1-5")
     ap.add_argument("--heads", type=int, default=0,
                     help="keep only the first N heads (a smaller case for profiling)")
     return ap.parse_args()
@@ -387,6 +391,105 @@ def time_bwd(wl, dw, meta, out, lse, err, stream, flop_fwd, iters=5):
             "note": "flop = 2.5 x forward flop over computed blocks; events around each call"}
 
 
+def time_forward(dw, meta, err, stream, ws, warmup=5, iters=20):
+    """Median of `iters` CUDA-event-timed forward calls (scheduling pass +
+    attention kernel) after `warmup` untimed ones, and the same for the metadata
+    kernel (K-META), on the launching stream."""
+    import torch
+    out = torch.empty_like(dw.q)
+    lse = None
+    for _ in range(warmup):
+        dw.build_meta(meta, err_flag=err, stream=stream)
+        out, lse = dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=ws, stream=stream)
+    torch.cuda.synchronize(dw.q.device)
+    f_ms, m_ms = [], []
+    for _ in range(iters):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        dw.build_meta(meta, err_flag=err, stream=stream)
+        e[1].record(stream)
+        dw.forward(meta, out=out, lse=lse, err_flag=err, workspace=ws, stream=stream)
+        e[2].record(stream)
+        torch.cuda.synchronize(dw.q.device)
+        m_ms.append(e[0].elapsed_time(e[1]))
+        f_ms.append(e[1].elapsed_time(e[2]))
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(err.item())}")
+    return statistics.median(f_ms), statistics.median(m_ms)
+
+
+def per_config(cfgs, dev, peak, stream):
+    """Forward and K-META of further workloads, each on its full seeded inputs
+    (median of 20 CUDA-event-timed runs after 5 warm-ups)."""
+    import torch
+    import block_sparse_flashattention_gb300 as bsa
+    from workloads import make_workload
+    from workloads.device import DeviceWorkload, computed_blocks, meta_to_numpy
+    res = {}
+    for cfg in cfgs:
+        wl = make_workload(cfg)
+        dw = DeviceWorkload(wl, dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        meta = dw.build_meta(err_flag=err, stream=stream)
+        ws = bsa.alloc_workspace(meta, dev)
+        torch.cuda.synchronize(dev)
+        blocks = computed_blocks(meta_to_numpy(meta))
+        flop = blocks * flop_per_tile(wl.D)
+        f_ms, m_ms = time_forward(dw, meta, err, stream, ws)
+        tf = flop / (f_ms * 1e-3) / 1e12
+        res[str(cfg)] = {"workload": wl.name, "computed_tiles": blocks, "flop": flop,
+                         "fwd_ms": f_ms, "tflops": tf, "frac": tf / peak, "meta_ms": m_ms,
+                         "timing": "median of 20 CUDA-event-timed calls after 5 warm-ups"}
+        del dw, meta, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def oracle_timing(cpu_seconds):
+    """The oracle (fp64, plain C) as it stands, on the host cores: the metadata
+    oracle against nothing but the clock on every config; the forward oracle over
+    whole configs 1-3 (measured) and configs 4-5 (extrapolated from a sample of
+    whole Q tiles of head 0 at the sampled rate), with all threads and with one."""
+    import numpy as np
+    import oracle
+    from workloads import make_workload
+    threads = oracle.default_threads()
+    res = {"threads": threads, "configs": {}}
+    sample_s = max(2.0, cpu_seconds / 4)
+    for cfg in (1, 2, 3, 4, 5):
+        wl = make_workload(cfg)
+        q, k, v = wl.qkv()
+        t0 = time.perf_counter()
+        meta = oracle.build_meta(wl, threads=threads)
+        meta_s = time.perf_counter() - t0
+        cnt = int(meta["full_cnt"].sum() + meta["mask_cnt"].sum())
+        flop = cnt * flop_per_tile(wl.D)
+        e = {"meta_oracle_s": meta_s, "computed_tiles": cnt, "flop": flop}
+        if cfg <= 3:
+            t0 = time.perf_counter()
+            oracle.fwd(wl, q, k, v, meta, threads=threads)
+            fwd_s = time.perf_counter() - t0
+            e.update(fwd_oracle_s=fwd_s, fwd_oracle_tflops=flop / fwd_s / 1e12,
+                     fwd_oracle_kind="measured, whole config")
+        else:
+            rate, _, desc = cpu_baseline(wl, q, k, v, sample_s, threads=threads)
+            e.update(fwd_oracle_s=flop / (rate * 1e12), fwd_oracle_tflops=rate,
+                     fwd_oracle_kind="extrapolated from a sample: " + desc)
+        if cfg <= 2:
+            t0 = time.perf_counter()
+            oracle.fwd(wl, q, k, v, meta, threads=1)
+            one_s = time.perf_counter() - t0
+            e.update(fwd_oracle_1thread_s=one_s, fwd_oracle_1thread_tflops=flop / one_s / 1e12,
+                     fwd_oracle_1thread_kind="measured, whole config")
+        else:
+            rate1, _, desc1 = cpu_baseline(wl, q, k, v, sample_s / 2, threads=1)
+            e.update(fwd_oracle_1thread_s=flop / (rate1 * 1e12), fwd_oracle_1thread_tflops=rate1,
+                     fwd_oracle_1thread_kind="extrapolated from a sample: " + desc1)
+        res["configs"][str(cfg)] = e
+        del q, k, v, meta
+    return res
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -426,7 +529,7 @@ def run_native(args):
     import torch
 
     import block_sparse_flashattention_gb300 as bsa
-    from tests.gpu_run import DeviceWorkload, meta_to_numpy, computed_blocks
+    from workloads.device import DeviceWorkload, meta_to_numpy, computed_blocks
     from workloads import make_workload
 
     ws, rank, local = dist_env()
@@ -588,13 +691,16 @@ def run_native(args):
     meta_formats = time_meta_formats(wl, dw, meta, err, stream) if not args.no_meta_formats else None
     proxy_ab = time_proxy(wl, dw, err, stream) if not args.no_meta_formats else None
     bwd = time_bwd(wl, dw, meta, out, lse, err, stream, flop_step) if not args.no_bwd else None
+    peaks, peak_src = measured_peaks()
+    others = [c for c in (3, 5) if c != args.config]
+    cfg_lines = (per_config(others, dev, float(peaks["bf16_tflops"]), stream)
+                 if not args.no_per_config and not args.heads else None)
 
     if rank != 0:
         if pg:
             pg.destroy_process_group()
         return
 
-    peaks, peak_src = measured_peaks()
     fwd_mean = statistics.mean(fwd_ms)
     achieved = flop_step / (fwd_mean * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
@@ -618,7 +724,11 @@ def run_native(args):
         k_np = hk.numpy().view(np.uint16)
         v_np = hv.numpy().view(np.uint16)
         cval, cores, desc = cpu_baseline(wl, q_np, k_np, v_np, args.cpu_seconds)
-        cpu = {"value": cval, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cval1, _, desc1 = cpu_baseline(wl, q_np, k_np, v_np, args.cpu_seconds / 3, threads=1)
+        cpu = {"value": cval, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "cores_1": {"value": cval1, "unit": UNIT, "cores": 1, "sample": desc1}}
+        if not args.no_oracle_timing:
+            cpu["oracle_timing"] = oracle_timing(args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -644,6 +754,7 @@ def run_native(args):
         "meta_formats": meta_formats,
         "proxy_ab": proxy_ab,
         "bwd": bwd if bwd is None or "ms" not in bwd else dict(bwd, frac=bwd["tflops"] / peak),
+        "per_config": cfg_lines,
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }
