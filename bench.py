@@ -445,6 +445,36 @@ def per_config(cfgs, dev, peak, stream):
     return res
 
 
+def time_sparse_blocks(wl, dw, meta, dev, stream, peak):
+    """A/B on a workload with a native sparse-block map (config 4: 256-token
+    blocks): the metadata kernel and the forward fed lists per 256 x 256 block
+    against the same fed per-tile lists, on the same device inputs (median of 20
+    CUDA-event-timed calls after 5 warm-ups each)."""
+    import copy
+    import torch
+    import block_sparse_flashattention_gb300 as bsa
+    from workloads.configs import as_sparse_blocks
+    from workloads.device import computed_blocks, meta_to_numpy
+    w2 = as_sparse_blocks(wl)
+    dw2 = copy.copy(dw)
+    dw2.wl = w2
+    dw2.block_map = torch.from_numpy(w2.block_map).to(dev)
+    dw2.vl = torch.from_numpy(w2.kv_valid_len).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    meta2 = dw2.build_meta(err_flag=err, stream=stream)
+    ws1, ws2 = bsa.alloc_workspace(meta, dev), bsa.alloc_workspace(meta2, dev)
+    torch.cuda.synchronize(dev)
+    flop = computed_blocks(meta_to_numpy(meta)) * flop_per_tile(wl.D)
+    f1, m1 = time_forward(dw, meta, err, stream, ws1)
+    f2, m2 = time_forward(dw2, meta2, err, stream, ws2)
+    return {"per_tile": {"fwd_ms": f1, "meta_ms": m1, "tflops": flop / (f1 * 1e-3) / 1e12,
+                         "list_entries": int(meta.full_idx.numel())},
+            "blocks_256x256": {"fwd_ms": f2, "meta_ms": m2, "tflops": flop / (f2 * 1e-3) / 1e12,
+                               "frac": flop / (f2 * 1e-3) / 1e12 / peak,
+                               "list_entries": int(meta2.full_idx.numel())},
+            "note": "same inputs and outputs; FLOP of the 128 x 128 tiles computed"}
+
+
 def oracle_timing(cpu_seconds):
     """The oracle (fp64, plain C) as it stands, on the host cores: the metadata
     oracle against nothing but the clock on every config; the forward oracle over
@@ -695,6 +725,8 @@ def run_native(args):
     others = [c for c in (3, 5) if c != args.config]
     cfg_lines = (per_config(others, dev, float(peaks["bf16_tflops"]), stream)
                  if not args.no_per_config and not args.heads else None)
+    blocks_ab = (time_sparse_blocks(wl, dw, meta, dev, stream, float(peaks["bf16_tflops"]))
+                 if "logical_map" in wl.extra and not args.heads and not args.no_per_config else None)
 
     if rank != 0:
         if pg:
@@ -755,6 +787,7 @@ def run_native(args):
         "proxy_ab": proxy_ab,
         "bwd": bwd if bwd is None or "ms" not in bwd else dict(bwd, frac=bwd["tflops"] / peak),
         "per_config": cfg_lines,
+        "sparse_blocks": blocks_ab,
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
         "clocks": clocks,
     }

@@ -40,10 +40,12 @@ def _cdiv(a: int, b: int) -> int:
 
 def alloc_meta(B: int, H: int, *, varlen: bool = False, seqlen_q: int = 0, seqlen_k: int = 0,
                total_m_blocks: int = 0, total_n_blocks: int = 0, max_num_n: int = 0,
-               device="cuda") -> Meta:
+               tile_m: int = TILE, tile_n: int = TILE, device="cuda") -> Meta:
     """Allocates the metadata tensors.
 
-    Batched: pass seqlen_q / seqlen_k (per sequence).  Varlen: pass
+    Batched: pass seqlen_q / seqlen_k (per sequence); tile_m / tile_n give the
+    listed block size (128 x 128 tiles, or sparse blocks of 256 x 128 or
+    256 x 256 tokens, whose lists the forward walks directly).  Varlen: pass
     total_m_blocks, total_n_blocks (sum of num_m(b) and of num_m(b) * num_n(b))
     and max_num_n (row stride of kv_valid_len, at least the largest num_n(b))."""
     import torch
@@ -57,12 +59,12 @@ def alloc_meta(B: int, H: int, *, varlen: bool = False, seqlen_q: int = 0, seqle
                     total_n_blocks=total_n_blocks,
                     cu_total_m_blocks=torch.empty(B + 1, **i32),
                     cu_block_idx_offsets=torch.empty(B + 1, **i32))
-    nm, nn = _cdiv(seqlen_q, TILE), _cdiv(seqlen_k, TILE)
+    nm, nn = _cdiv(seqlen_q, tile_m), _cdiv(seqlen_k, tile_n)
     return Meta(full_cnt=torch.empty((B, H, nm), **i32),
                 full_idx=torch.empty((B, H, nm, nn), **i32),
                 mask_cnt=torch.empty((B, H, nm), **i32),
                 mask_idx=torch.empty((B, H, nm, nn), **i32), varlen=0, B=B, H=H, num_m=nm,
-                num_n=nn)
+                num_n=nn, tile_m=tile_m, tile_n=tile_n)
 
 
 def alloc_workspace(meta: Meta, device="cuda"):

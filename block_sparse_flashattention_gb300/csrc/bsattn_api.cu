@@ -41,10 +41,26 @@ bsattn_status check_mask(bsattn_mask_kind kind, const bsattn_mask_params *mp) {
     }
 }
 
+// Metadata listed per 128 x 128 tile (every entry point), or, batched only, per
+// sparse block of two Q tiles and one or two KV tiles (bsattn_build_meta and the
+// forward).
+bool per_tile(const bsattn_meta *m) { return m->tile_m == kTile && m->tile_n == kTile; }
+bool per_block(const bsattn_meta *m) {
+    return !m->varlen && m->tile_m == 2 * kTile && (m->tile_n == kTile || m->tile_n == 2 * kTile);
+}
+
+// Work units of the forward: pairs of consecutive Q tiles of a head; with
+// metadata per sparse block of two Q tiles, one unit per block.
+long long fwd_units(const bsattn_meta *m) {
+    if (per_block(m)) return (long long)m->H * m->B * m->num_m;
+    const long long total_m = m->varlen ? (long long)m->total_m_blocks : (long long)m->B * m->num_m;
+    return (long long)m->H * cdiv(total_m, 2);
+}
+
 // Common checks on the metadata descriptor.
 bsattn_status check_meta(const bsattn_meta *m) {
     if (!m) return BSATTN_ERR_INVALID_ARG;
-    if (m->tile_m != kTile || m->tile_n != kTile) return BSATTN_ERR_UNSUPPORTED;
+    if (!per_tile(m) && !per_block(m)) return BSATTN_ERR_UNSUPPORTED;
     if (m->B <= 0 || m->H <= 0) return BSATTN_ERR_INVALID_ARG;
     if (!m->full_cnt || !m->full_idx || !m->mask_cnt || !m->mask_idx) return BSATTN_ERR_INVALID_ARG;
     if (m->varlen != 0 && m->varlen != 1) return BSATTN_ERR_INVALID_ARG;
@@ -127,11 +143,13 @@ bsattn_status build_meta_impl(bsattn::MetaParams p, const int32_t *cu_seqlens_q,
     } else {
         if (cu_seqlens_q || cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
         if (seqlen_q < 0 || seqlen_k < 0) return BSATTN_ERR_INVALID_ARG;
-        if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+        if (meta->num_m != cdiv(seqlen_q, meta->tile_m) || meta->num_n != cdiv(seqlen_k, meta->tile_n))
             return BSATTN_ERR_INVALID_ARG;
         if ((long long)meta->B * seqlen_q > INT32_MAX || (long long)meta->B * seqlen_k > INT32_MAX)
             return BSATTN_ERR_INVALID_ARG;
     }
+    p.tile_q = meta->tile_m;
+    p.tile_k = meta->tile_n;
     p.seqlen_q = seqlen_q;
     p.seqlen_k = seqlen_k;
     p.cu_q = cu_seqlens_q;
@@ -198,15 +216,22 @@ bsattn_status fwd_impl(const void *q, const void *k, const void *v, int32_t B, i
         p.lse_row_stride = seqlen_q;
     } else {
         if (cu_seqlens_q || cu_seqlens_k) return BSATTN_ERR_INVALID_ARG;
-        if (meta->num_m != cdiv(seqlen_q, kTile) || meta->num_n != cdiv(seqlen_k, kTile))
+        if (meta->num_m != cdiv(seqlen_q, meta->tile_m) || meta->num_n != cdiv(seqlen_k, meta->tile_n))
             return BSATTN_ERR_INVALID_ARG;
         rows_q = (long long)B * seqlen_q;
         rows_k = (long long)B * seqlen_k;
-        p.total_m = B * meta->num_m;
-        p.num_m = meta->num_m;
-        p.num_n = meta->num_n;
+        p.num_m = (int)cdiv(seqlen_q, kTile);
+        p.num_n = (int)cdiv(seqlen_k, kTile);
+        // a list row per sparse Q block is one work unit: every block whole
+        if (per_block(meta) && (p.num_m & 1)) return BSATTN_ERR_UNSUPPORTED;
+        if ((long long)B * p.num_m > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
+        p.total_m = B * p.num_m;
         p.lse_row_stride = seqlen_q;
     }
+    p.list_q_tiles = meta->tile_m / kTile;
+    p.list_kv_tiles = meta->tile_n / kTile;
+    p.list_m = meta->num_m;
+    p.list_n = meta->num_n;
     if (rows_q > INT32_MAX || rows_k > INT32_MAX) return BSATTN_ERR_INVALID_ARG;
     p.seqlen_q = seqlen_q;
     p.seqlen_k = seqlen_k;
@@ -329,9 +354,7 @@ bsattn_status bsattn_fwd_workspace_size(const bsattn_meta *meta, size_t *bytes) 
     *bytes = 0;
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
-    const long long total_m =
-        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
-    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    const long long units = fwd_units(meta);
     if (units <= 0 || units > bsattn::kMaxScheduledUnits) return BSATTN_OK;
     *bytes = (size_t)(kWorkspaceHeader + 4 * units);
     return BSATTN_OK;
@@ -373,6 +396,7 @@ bsattn_status bsattn_build_meta_blocks(const uint8_t *block_map, int32_t q_block
     if (q_block_tiles < 1 || kv_block_tiles < 1 || q_block_tiles > 1024 || kv_block_tiles > 1024)
         return BSATTN_ERR_INVALID_ARG;
     if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched layouts only
+    if (!per_tile(meta)) return BSATTN_ERR_UNSUPPORTED;  // writes per-tile lists
     if (kv_valid_len_blocks && !kv_valid_len_tiles) return BSATTN_ERR_INVALID_ARG;
     bsattn::MetaParams p = {};
     p.src = bsattn::kSrcByteMap;
@@ -445,7 +469,7 @@ bsattn_status bsattn_fwd_proxy(const void *q, const void *k, const void *v, int3
                                void *workspace, size_t workspace_bytes, int32_t *err_flag,
                                void *stream) {
     if (!meta) return BSATTN_ERR_INVALID_ARG;
-    if (meta->varlen) return BSATTN_ERR_UNSUPPORTED;  // batched only
+    if (meta->varlen || !per_tile(meta)) return BSATTN_ERR_UNSUPPORTED;  // batched, per tile
     if (!sel_words || !k_sum || !v_sum) return BSATTN_ERR_INVALID_ARG;
     if (!aligned16(k_sum) || !aligned16(v_sum)) return BSATTN_ERR_INVALID_ARG;
     if (words_per_row <= 0 || (long long)words_per_row * 32 < meta->num_n) return BSATTN_ERR_INVALID_ARG;
@@ -459,6 +483,7 @@ bsattn_status bsattn_fwd_proxy(const void *q, const void *k, const void *v, int3
 bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
+    if (!per_tile(meta)) return BSATTN_ERR_UNSUPPORTED;
     if (!bytes) return BSATTN_ERR_INVALID_ARG;
     if (meta->varlen && meta->num_n <= 0) return BSATTN_ERR_INVALID_ARG;
     *bytes = bwd_layout(meta).total;
@@ -475,6 +500,7 @@ bsattn_status bsattn_bwd(const void *q, const void *k, const void *v, const void
                          int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
+    if (!per_tile(meta)) return BSATTN_ERR_UNSUPPORTED;
     if ((st = check_mask(kind, mp)) != BSATTN_OK) return st;
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
         return BSATTN_ERR_INVALID_ARG;
@@ -648,9 +674,7 @@ extern "C" bsattn_status bsattn_fwd_static_scratch(
     float *lse, int32_t *err_flag, void *stream) {
     bsattn_status st = check_meta(meta);
     if (st != BSATTN_OK) return st;
-    const long long total_m =
-        meta->varlen ? (long long)meta->total_m_blocks : (long long)meta->B * meta->num_m;
-    const long long units = (long long)meta->H * cdiv(total_m, 2);
+    const long long units = fwd_units(meta);
     if (units > BSATTN_STATIC_SCRATCH_UNITS) return BSATTN_ERR_CAPACITY;
     void *scratch = nullptr;
     if ((st = static_scratch_address(&scratch)) != BSATTN_OK) return st;

@@ -562,7 +562,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams &p, const uint32_t 
 // build carries none of that code.  kPolled: pipeline waits poll without
 // suspending and give up after p.wait_limit cycles (the build a lowered wait
 // limit runs; the waits of the default build use their fixed one-second limit).
-template <int D, bool kProxy, bool kPolled>
+// kBlocks: lists per sparse block of two Q tiles (one list row per unit), each
+// entry covering p.list_kv_tiles KV tiles; the per-tile builds carry none of it.
+template <int D, bool kProxy, bool kPolled, bool kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -660,8 +662,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else ++qn1;
                 }
                 Cursor cm[2], cf[2];
+                // With lists per sparse Q block the unit is one block: its two Q
+                // tiles walk the block's one list, each entry's KV tiles in turn.
+                constexpr bool block_lists = kBlocks;
                 for (int t = 0; t < 2; ++t) {
-                    if (ti[t].valid) {
+                    if (block_lists) {
+                        const long long idx_at =
+                            (((long long)ti[0].b * p.H + h) * p.list_m + (ti[0].m >> 1)) * p.list_n;
+                        if (t == 0 && ti[0].valid) {
+                            cur_init(cm[0], p.mask_idx + idx_at, d.cnt[0], d.e0[0], d.e1[0], p.list_n, p.err);
+                            cur_init(cf[0], p.full_idx + idx_at, d.cnt[1], d.e0[1], d.e1[1], p.list_n, p.err);
+                        } else {
+                            cm[t].head = cf[t].head = -1;
+                            cm[t].cnt = cf[t].cnt = 0;
+                            cm[t].pos = cf[t].pos = 0;
+                        }
+                    } else if (ti[t].valid) {
                         cur_init(cm[t], p.mask_idx + ti[t].idx_at, d.cnt[2 * t], d.e0[2 * t],
                                  d.e1[2 * t], ti[t].nn, p.err);
                         cur_init(cf[t], p.full_idx + ti[t].idx_at, d.cnt[2 * t + 1], d.e0[2 * t + 1],
@@ -672,7 +688,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                         cm[t].pos = cf[t].pos = 0;
                     }
                 }
-                while (true) {
+                while (block_lists) {
+                    // next entry of the block's lists: KV block c, its tiles from the
+                    // top down as dual items (both Q tiles share the block's list)
+                    const int c = max(cm[0].head, cf[0].head);
+                    if (c < 0) break;
+                    const bool mblk = cm[0].head == c;
+                    const int kvt = p.list_kv_tiles;
+                    int vlb = kvt * kTile;  // valid keys of the block (mask blocks only)
+                    if (mblk) {
+                        if (p.vl)
+                            vlb = cm[0].pos == 0 ? d.vl[0] : __ldg(p.vl + (long long)ti[0].b * p.vl_stride + c);
+                        cur_advance(cm[0], p.list_n, p.err);
+                    } else {
+                        cur_advance(cf[0], p.list_n, p.err);
+                    }
+                    const bool list_done = max(cm[0].head, cf[0].head) < 0;
+                    // keys of tile c * kvt + j that may be kept: the sequence end, and on
+                    // a mask block the valid length, tile j of the block keeping
+                    // clamp(v - 128 j, 0, 128) of the block's v valid keys
+                    const int n_lo = c * kvt;
+                    int lim[2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int n = n_lo + j;
+                        int l = (j < kvt && n < ti[0].nn) ? min(kTile, ti[0].sk - n * kTile) : 0;
+                        if (mblk) l = min(l, max(0, min(kTile, vlb - j * kTile)));
+                        lim[j] = l;
+                    }
+#pragma unroll
+                    for (int j = 1; j >= 0; --j) {
+                        if (lim[j] <= 0) continue;  // no key of this tile is kept
+                        const int n = n_lo + j;
+                        const uint32_t both = ti[1].valid ? 3u : 1u;  // kPart1 = 2 kPart0
+                        Item it;
+                        it.krow = ti[0].krow0 + n * kTile;
+                        it.n0 = n;
+                        it.n1 = ti[1].valid ? n : -1;
+                        it.flags = both;  // kPart0 | kPart1
+                        // mask_mod runs on mask blocks; without one, a tile whose keys
+                        // are all valid needs no mask at all
+                        if (mblk && !(p.kind == BSATTN_MASK_NONE && lim[j] == kTile)) it.flags |= both * kMask0;
+                        if ((n + 1) * kTile > ti[0].sk) it.flags |= both * kBound0;
+                        if (list_done && (j == 0 || lim[0] <= 0)) it.flags |= both * kLast0;
+                        it.lim0 = it.lim1 = lim[j];
+                        it.pad0 = it.pad1 = 0;
+                        const uint32_t ks = kc % C::kStagesK;
+                        if (!mbar_wait_lim<kPolled>(bar(C::bKE + ks), ((kc / C::kStagesK) & 1) ^ 1, abort_flag,
+                                                    p.err, BSATTN_FLAG_TIMEOUT, p.wait_limit))
+                            goto producer_done;
+                        items[ks] = it;
+                        mbar_arrive_expect_tx_lead(lead, bar(C::bKF + ks), 2 * C::kTileBytes);
+                        for (int x = 0; x < C::kSub; ++x)
+                            tma_load_3d_lead(lead, sK + ks * C::kTileBytes + x * kSubTileBytes, &tk,
+                                             bar(C::bKF + ks), x * 64, h, it.krow);
+                        ++kc;
+                        const uint32_t vs = vc % C::kStagesV;
+                        if (!mbar_wait_lim<kPolled>(bar(C::bVE + vs), ((vc / C::kStagesV) & 1) ^ 1, abort_flag,
+                                                    p.err, BSATTN_FLAG_TIMEOUT, p.wait_limit)) {
+                            mbar_complete_tx_lead(lead, bar(C::bKF + ks), C::kTileBytes);
+                            goto producer_done;
+                        }
+                        for (int x = 0; x < C::kSub; ++x)
+                            tma_load_3d_lead(lead, sV + vs * C::kTileBytes + x * kSubTileBytes, &tv,
+                                             bar(C::bKF + ks), x * 64, h, it.krow);
+                        ++vc;
+                    }
+                }
+                while (!block_lists) {
                     const int c0 = max(cm[0].head, cf[0].head);
                     const int c1 = max(cm[1].head, cf[1].head);
                     if (c0 < 0 && c1 < 0) break;
@@ -1048,16 +1131,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const TileInfo ti = tile_info(p, h, 2 * pr + t, lead ? p.err : nullptr);
                     d.ti[t] = ti;
                     int cm = 0, cf = 0, m0 = -1, m1 = -1, f0 = -1, f1 = -1, vl = kTile;
-                    if (ti.valid) {
-                        cm = __ldg(p.mask_cnt + ti.cnt_at);
-                        cf = __ldg(p.full_cnt + ti.cnt_at);
-                        m0 = __ldg(p.mask_idx + ti.idx_at);
-                        f0 = __ldg(p.full_idx + ti.idx_at);
-                        if (ti.nn > 1) {
-                            m1 = __ldg(p.mask_idx + ti.idx_at + 1);
-                            f1 = __ldg(p.full_idx + ti.idx_at + 1);
+                    // the lists of tile t, or, with lists per sparse Q block, the
+                    // block's one list (read for tile 0; tile 1 has none of its own)
+                    long long cnt_at = ti.cnt_at, idx_at = ti.idx_at;
+                    int nn = ti.nn;
+                    const bool has_list = ti.valid && (!kBlocks || t == 0);
+                    if constexpr (kBlocks) {
+                        cnt_at = ((long long)ti.b * p.H + h) * p.list_m + (ti.m >> 1);
+                        idx_at = cnt_at * p.list_n;
+                        nn = p.list_n;
+                    }
+                    if (has_list) {
+                        cm = __ldg(p.mask_cnt + cnt_at);
+                        cf = __ldg(p.full_cnt + cnt_at);
+                        m0 = __ldg(p.mask_idx + idx_at);
+                        f0 = __ldg(p.full_idx + idx_at);
+                        if (nn > 1) {
+                            m1 = __ldg(p.mask_idx + idx_at + 1);
+                            f1 = __ldg(p.full_idx + idx_at + 1);
                         }
-                        if (p.vl && cm > 0 && m0 >= 0 && m0 < ti.nn)
+                        if (p.vl && cm > 0 && m0 >= 0 && m0 < nn)
                             vl = __ldg(p.vl + (long long)ti.b * p.vl_stride + m0);
                     }
                     d.cnt[2 * t] = cm;
@@ -1094,7 +1187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Work of one Q tile = its listed KV tiles (counts clamped to [0, 2^15)).
+// Work of one Q tile = its listed KV tiles (counts clamped to [0, 2^15)).  With
+// lists per sparse Q block the block's list counts for its first tile only.
 __device__ __forceinline__ int tile_weight(const FwdParams &p, int h, int T) {
     if (T >= p.total_m) return 0;
     long long at;
@@ -1102,9 +1196,14 @@ __device__ __forceinline__ int tile_weight(const FwdParams &p, int h, int T) {
         at = (long long)h * p.total_m + T;
     } else {
         const int b = T / p.num_m, m = T - b * p.num_m;
-        at = ((long long)b * p.H + h) * p.num_m + m;
+        if (p.list_q_tiles == 2) {
+            if (m & 1) return 0;
+            at = ((long long)b * p.H + h) * p.list_m + (m >> 1);
+        } else {
+            at = ((long long)b * p.H + h) * p.num_m + m;
+        }
     }
-    const int w = max(__ldg(p.full_cnt + at), 0) + max(__ldg(p.mask_cnt + at), 0);
+    const int w = (max(__ldg(p.full_cnt + at), 0) + max(__ldg(p.mask_cnt + at), 0)) * p.list_kv_tiles;
     return min(w, 32767);
 }
 
@@ -1156,7 +1255,7 @@ __global__ void __launch_bounds__(1024, 1) bsattn_schedule_kernel(const __grid_c
     }
 }
 
-template <int D, bool kProxy, bool kPolled>
+template <int D, bool kProxy, bool kPolled, bool kBlocks>
 cudaError_t prepare_fwd_kernel() {
     using C = Cfg<D>;
     static int attr_set_for_device[64] = {0};
@@ -1168,10 +1267,10 @@ cudaError_t prepare_fwd_kernel() {
         // The register split inside the kernel assumes exactly kLaunchRegs per
         // thread at launch; refuse to run a build where that does not hold.
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D, kProxy, kPolled>);
+        e = cudaFuncGetAttributes(&fa, bsattn_fwd_kernel<D, kProxy, kPolled, kBlocks>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, kProxy, kPolled>,
+        e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, kProxy, kPolled, kBlocks>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set_for_device[dev] = 1;
@@ -1179,14 +1278,14 @@ cudaError_t prepare_fwd_kernel() {
     return cudaSuccess;
 }
 
-template <int D, bool kProxy, bool kPolled>
+template <int D, bool kProxy, bool kPolled, bool kBlocks>
 cudaError_t launch_fwd_kernel(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, const CUtensorMap &tks, const CUtensorMap &tvs,
                               int grid, cudaStream_t stream) {
-    cudaError_t e = prepare_fwd_kernel<D, kProxy, kPolled>();
+    cudaError_t e = prepare_fwd_kernel<D, kProxy, kPolled, kBlocks>();
     if (e != cudaSuccess) return e;
-    bsattn_fwd_kernel<D, kProxy, kPolled><<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(p, tq, tk, tv, tks,
-                                                                                          tvs);
+    bsattn_fwd_kernel<D, kProxy, kPolled, kBlocks>
+        <<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
     return cudaGetLastError();
 }
 
@@ -1210,10 +1309,12 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
     const int grid = p.num_units < num_sms ? p.num_units : num_sms;
     // A wait limit below the default (a test lowering it) runs the build whose
     // waits poll against that limit; the proxy build keeps its fixed limit.
-    if (p.proxy) return launch_fwd_kernel<D, true, false>(p, tq, tk, tv, tks, tvs, grid, stream);
+    // Lists per sparse block run their own build (with the default limit).
+    if (p.proxy) return launch_fwd_kernel<D, true, false, false>(p, tq, tk, tv, tks, tvs, grid, stream);
+    if (p.list_q_tiles == 2) return launch_fwd_kernel<D, false, false, true>(p, tq, tk, tv, tks, tvs, grid, stream);
     if (p.wait_limit < kDefaultWaitLimitCycles)
-        return launch_fwd_kernel<D, false, true>(p, tq, tk, tv, tks, tvs, grid, stream);
-    return launch_fwd_kernel<D, false, false>(p, tq, tk, tv, tks, tvs, grid, stream);
+        return launch_fwd_kernel<D, false, true, false>(p, tq, tk, tv, tks, tvs, grid, stream);
+    return launch_fwd_kernel<D, false, false, false>(p, tq, tk, tv, tks, tvs, grid, stream);
 }
 
 }  // namespace

@@ -34,6 +34,8 @@ struct MetaParams {
     int32_t *vl_tiles_out;
     int varlen, B, H;
     int num_m, num_n;              // batched sizes (varlen: num_n = kv_valid_len stride)
+    int tile_q, tile_k;            // rows / keys of a listed block: 128, or (batched) a
+                                   // sparse block of two tiles
     int total_m, total_n;          // varlen packed sizes as allocated by the caller
     int seqlen_q, seqlen_k;        // batched
     const int32_t *cu_q, *cu_k;    // varlen [B+1]
@@ -50,8 +52,12 @@ struct FwdParams {
     int varlen, B, H;
     int seqlen_q, seqlen_k;        // batched per-sequence lengths
     const int32_t *cu_q, *cu_k;    // varlen [B+1]
-    int num_m, num_n;              // batched
+    int num_m, num_n;              // batched: 128-row tiles per sequence
     int total_m, total_n;          // Q tiles per head over the batch; varlen idx row size
+    // Lists per sparse block (batched): list_q_tiles = 2 Q tiles share a list row
+    // (one work unit), each entry covers list_kv_tiles (1 or 2) KV tiles; list_m
+    // rows per sequence, list_n entries per row.  list_q_tiles = 1: per-tile lists.
+    int list_q_tiles, list_kv_tiles, list_m, list_n;
     const int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;
     const int32_t *cu_tm, *cu_off; // varlen
     const int32_t *vl;

@@ -86,9 +86,10 @@ __device__ __forceinline__ long long tile_valid_len(const MetaParams &p, int b, 
     return v < 0 ? 0 : (v > kTile ? kTile : v);
 }
 
-// 0 = drop, 1 = mask list, 2 = full list.
+// 0 = drop, 1 = mask list, 2 = full list, for listed block n (p.tile_k keys) of
+// the row's rectangle of query rows.
 __device__ int classify(const MetaParams &p, const RowGeom &g, int n) {
-    const long long j_lo = (long long)n * kTile, j_end = j_lo + kTile;
+    const long long j_lo = (long long)n * p.tile_k, j_end = j_lo + p.tile_k;
     long long j_hi = j_end < g.sk ? j_end : g.sk;
     if (p.vl) {
         const long long lim = j_lo + tile_valid_len(p, g.b, n);
@@ -162,8 +163,8 @@ __global__ void __launch_bounds__(256) bsattn_meta_classify_kernel(MetaParams p)
         g.b = (int)(bh / p.H);
         g.sk = p.seqlen_k;
         const long long sq = p.seqlen_q;
-        g.i_min = (long long)m * kTile;
-        g.i_max = (g.i_min + kTile < sq ? g.i_min + kTile : sq) - 1;
+        g.i_min = (long long)m * p.tile_q;
+        g.i_max = (g.i_min + p.tile_q < sq ? g.i_min + p.tile_q : sq) - 1;
         g.qbase = (long long)g.b * p.seqlen_q;
         g.kbase = (long long)g.b * p.seqlen_k;
         nn = p.num_n;

@@ -100,7 +100,22 @@ typedef struct {
  *   num_m               unused; num_n = the row stride of kv_valid_len (at least
  *                       the largest num_n(b))
  * Each index row lists KV block ids in descending order; entries at and after
- * the row's count are -1.  tile_m = tile_n = 128 in this build.
+ * the row's count are -1.
+ *
+ * tile_m x tile_n is the size of a listed block: 128 x 128 (one tile; every
+ * entry point), or, batched only, a sparse block of two Q tiles and one or two
+ * KV tiles: 256 x 128 or 256 x 256 ("[CuTe,Flex] varlen blocksparsity",
+ * flash-attention #2224: lists per q_subtile_factor x tile_m sparse block;
+ * "[feat] VSA-256 fastpath on Blackwell via FA4 CuTe block-sparse attention",
+ * FastVideo #1354: 256-token blocks).  Then num_m = ceil(seqlen_q / tile_m),
+ * num_n = ceil(seqlen_k / tile_n), bsattn_build_meta classifies whole blocks
+ * (the token predicate over the block's query rows and keys), kv_valid_len
+ * holds one value per KV block ([B, num_n], tile j of a block keeping
+ * clamp(v - 128 j, 0, 128) keys), and bsattn_fwd walks the block lists
+ * directly: a block's two Q tiles form one work unit, each entry's KV tiles
+ * are visited in turn.  The forward then needs ceil(seqlen_q / 128) even (each
+ * Q block whole); bsattn_bwd, bsattn_fwd_proxy and bsattn_build_meta_blocks
+ * take 128 x 128 metadata only.  Other sizes -> BSATTN_ERR_UNSUPPORTED.
  */
 typedef struct {
     int32_t *full_cnt, *full_idx, *mask_cnt, *mask_idx;
@@ -114,11 +129,13 @@ typedef struct {
  * bsattn_build_meta -- boolean block map -> full / mask lists (and, for
  * varlen, the two offset tensors).
  *
- * Every selected KV tile n of row (b, h, m) is classified by the token
- * predicate P(i, j) = j < seqlen_k(b) && mask_mod(i, j) && (j - 128 n) <
- * kv_valid_len[b, n] over the tile's query rows i < seqlen_q(b) and its 128
- * keys j: true for every pair -> full list, for some pair -> mask list, for none
- * -> dropped.  Result is bit-exact and deterministic.
+ * Every selected KV block n of row (b, h, m) is classified by the token
+ * predicate P(i, j) = j < seqlen_k(b) && mask_mod(i, j) && (j - tile_n n) <
+ * kv_valid_len[b, n] over the row's query rows i < seqlen_q(b) (tile_m of them
+ * from tile_m m) and the block's tile_n keys j: true for every pair -> full list,
+ * for some pair -> mask list, for none -> dropped (tile_m = tile_n = 128 unless
+ * the metadata is per sparse block, see above).  Result is bit-exact and
+ * deterministic.
  *
  * block_map     device uint8; batched [B, H, num_m, num_n], varlen [H, total_n_blocks]
  *               in the packed layout above; nonzero = selected.
@@ -130,7 +147,7 @@ typedef struct {
  *               reach past them (or are negative) is rejected: its rows are not
  *               written and BSATTN_FLAG_BAD_SEQLENS is set.
  * kv_valid_len  optional device int32 [B, meta->num_n]: valid keys at the start
- *               of each KV tile (the rest of the tile is masked on mask blocks).
+ *               of each listed KV block (the rest of it is masked on mask blocks).
  * kind, mp      mask_mod (mp may be NULL unless the kind needs it).
  * meta          sizes in, device output pointers in; varlen also writes
  *               cu_total_m_blocks / cu_block_idx_offsets.  If the totals the

@@ -283,3 +283,33 @@ def test_bwd_workspace_size():
     with pytest.raises(bsa.BsattnError):
         bsa.bsattn_bwd_workspace_size(_meta(varlen=1, num_n=0, cu_total_m_blocks=FAKE,
                                             cu_block_idx_offsets=FAKE))
+
+
+def test_sparse_block_metadata_rules():
+    """Metadata per sparse block (tile_m 256, tile_n 256 or 128) is batched only;
+    the forward needs an even number of 128-row Q tiles per sequence (each unit
+    one whole block); the backward, the proxy forward and the block-map
+    expansion take per-tile metadata only."""
+    UNS = bsa.BSATTN_ERR_UNSUPPORTED
+    blk = dict(tile_m=256, tile_n=256, num_m=2, num_n=2)
+    # accepted sizes reach the device launch, which FAKE pointers cannot pass:
+    # they must not fail the host checks (any status but INVALID_ARG/UNSUPPORTED)
+    assert bsa.bsattn_fwd_workspace_size(_meta(**blk)) == 256 + 4 * 2 * 2
+    assert _fwd(meta=_meta(tile_m=256, tile_n=128, num_m=2, num_n=4), seqlen_q=512,
+                seqlen_k=512) not in (bsa.BSATTN_ERR_INVALID_ARG, UNS)
+    # an odd number of Q tiles (384 rows = 3 tiles): a unit would hold half a block
+    assert _fwd(meta=_meta(tile_m=256, tile_n=256, num_m=2, num_n=2), seqlen_q=384,
+                seqlen_k=512) == UNS
+    # sizes must follow the block size
+    assert _fwd(meta=_meta(**blk), seqlen_q=256, seqlen_k=512) == bsa.BSATTN_ERR_INVALID_ARG
+    # unsupported block shapes and layouts
+    assert _fwd(meta=_meta(tile_m=128, tile_n=256, num_m=4, num_n=2), seqlen_q=512,
+                seqlen_k=512) == UNS
+    assert _fwd(meta=_meta(tile_m=512, tile_n=512, num_m=1, num_n=1), seqlen_q=512,
+                seqlen_k=512) == UNS
+    assert _fwd(meta=_meta(varlen=1, cu_total_m_blocks=FAKE, cu_block_idx_offsets=FAKE, **blk),
+                cu_seqlens_q=FAKE, cu_seqlens_k=FAKE) == UNS
+    with pytest.raises(bsa.BsattnError):
+        bsa.bsattn_bwd_workspace_size(_meta(**blk))
+    assert bsa.bsattn_build_meta_blocks(FAKE, 2, 2, 512, 512, None, None, bsa.MASK_NONE, None,
+                                        _meta(**blk), stream=0) == UNS

@@ -137,10 +137,13 @@ def random_workload(seed: int, B: int, H: int, D: int, seqlens_q: List[int],
                     density: float = 0.5, kind: int = MASK_CAUSAL, window_left: int = 0,
                     sink_tokens: int = 0, prefix_len: int = 0, valid_len: bool = False,
                     n_docs: int = 3, scale: Optional[float] = None,
-                    force_diag: bool = True, name: str = "random") -> Workload:
+                    force_diag: bool = True, name: str = "random", tile_m: int = TILE,
+                    tile_n: int = TILE) -> Workload:
     """A seeded workload with Bernoulli(density) block maps.
 
     For batched workloads seqlens_q (and seqlens_k) must hold B equal lengths.
+    tile_m / tile_n: the listed block size (batched only when not 128), which the
+    map, the diagonal and the valid lengths (1..tile_n per block) refer to.
     """
     from . import uniform01, u64
     if seqlens_k is None:
@@ -154,7 +157,8 @@ def random_workload(seed: int, B: int, H: int, D: int, seqlens_q: List[int],
                   block_map=np.zeros(1, np.uint8), kind=kind,
                   scale=(1.0 / math.sqrt(D)) if scale is None else scale,
                   data_seed=seed, window_left=window_left, sink_tokens=sink_tokens,
-                  prefix_len=prefix_len)
+                  prefix_len=prefix_len, tile_m=tile_m, tile_n=tile_n)
+    assert not varlen or (tile_m == TILE and tile_n == TILE)
     mseed = seed + 1000
     if varlen:
         off = wl.map_row_offsets()
@@ -178,7 +182,7 @@ def random_workload(seed: int, B: int, H: int, D: int, seqlens_q: List[int],
     if valid_len:
         nn = wl.num_n
         r = u64(B * nn, mseed, S_VALID).reshape(B, nn)
-        wl.kv_valid_len = (1 + (r % TILE)).astype(np.int32)      # 1..128
+        wl.kv_valid_len = (1 + (r % tile_n)).astype(np.int32)    # 1..tile_n
     if kind == MASK_DOCUMENT:
         def docs(lengths, stream):
             out = []
@@ -298,6 +302,19 @@ def _cfg5() -> Workload:
 
 
 CONFIGS = {1: _cfg1, 2: _cfg2, 3: _cfg3, 4: _cfg4, 5: _cfg5}
+
+
+def as_sparse_blocks(wl: Workload) -> Workload:
+    """Config 4 stated at its native sparse-block size: the map per 256-token
+    logical block (240 x 240 per head) with one valid length per logical KV
+    block, listed as 256 x 256 blocks (q/k/v are the same draws)."""
+    from dataclasses import replace
+    logical = wl.extra["logical_map"]
+    return replace(wl, tile_m=2 * TILE, tile_n=2 * TILE,
+                   block_map=np.ascontiguousarray(logical[None]),
+                   kv_valid_len=np.ascontiguousarray(
+                       wl.extra["logical_block_valid_len"].reshape(wl.B, -1).astype(np.int32)),
+                   name=wl.name + "_256blocks")
 
 
 def with_heads(wl: Workload, heads: int) -> Workload:

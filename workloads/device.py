@@ -58,7 +58,8 @@ class DeviceWorkload:
             return bsa.alloc_meta(wl.B, wl.H, varlen=True, total_m_blocks=wl.total_m_blocks,
                                   total_n_blocks=wl.total_n_blocks, max_num_n=wl.num_n,
                                   device=self.device)
-        return bsa.alloc_meta(wl.B, wl.H, seqlen_q=sq, seqlen_k=sk, device=self.device)
+        return bsa.alloc_meta(wl.B, wl.H, seqlen_q=sq, seqlen_k=sk, tile_m=wl.tile_m,
+                              tile_n=wl.tile_n, device=self.device)
 
     def build_meta(self, meta=None, err_flag=None, stream=None):
         meta = meta or self.alloc_meta()
