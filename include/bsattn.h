@@ -446,8 +446,9 @@ bsattn_status bsattn_bwd_workspace_size(const bsattn_meta *meta, size_t *bytes);
  * BSATTN_FLAG_TIMEOUT in err_flag, waits for the copies and tensor-core products
  * it has already issued, frees its tensor memory and exits; out / lse are then
  * incomplete.  cycles <= 0 restores the default of 2^31 cycles (about one
- * second at 2 GHz).  bsattn_fwd_proxy keeps the default.  The setting is
- * process-wide and read when a call is made; always BSATTN_OK.
+ * second at 2 GHz).  bsattn_fwd_proxy, and bsattn_fwd with metadata listed
+ * per sparse block, keep the default.  The setting is process-wide and read
+ * when a call is made; always BSATTN_OK.
  */
 bsattn_status bsattn_testing_set_wait_limit(long long cycles);
 
