@@ -618,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // Launched as a dependent of the scheduling pass (or of whatever preceded it
+    // on the stream): nothing global is read or written before this point.
+    grid_dependency_wait();
 
     if (warp == 0) {
         regs_release<kCtrlRegs>();
@@ -1211,48 +1214,96 @@ __device__ __forceinline__ int tile_weight(const FwdParams &p, int h, int T) {
 // (units of equal work keep their head-major order, which keeps one head's K/V
 // resident in L2 while the CTAs work on it), and resets the claim counter.
 // Heaviest-first claiming is the longest-processing-time rule for list scheduling.
+//
+// A counting sort over 1024 work keys, split into kSchedChunks contiguous runs
+// of units: every run's key histogram, one exclusive scan over (key, run), then
+// each warp scatters its own run in unit order.  The attention kernel launched
+// after it starts at once and waits for its completion before its first claim.
 constexpr int kSchedBuckets = 1024;
-__global__ void __launch_bounds__(1024, 1) bsattn_schedule_kernel(const __grid_constant__ FwdParams p) {
-    __shared__ int start[kSchedBuckets];
-    extern __shared__ uint16_t key_of[];  // [num_units]: kSchedBuckets - 1 - min(work, 1023)
-    const int tid = threadIdx.x;
-    for (int b = tid; b < kSchedBuckets; b += blockDim.x) start[b] = 0;
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedChunks = kSchedThreads / 32;  // one run per warp
+constexpr size_t kSchedSmemBytes = (size_t)kSchedChunks * kSchedBuckets * sizeof(int);
+static_assert(kSchedThreads == kSchedBuckets, "one thread per work key in the scan");
+
+__device__ __forceinline__ int unit_key(const FwdParams &p, int u) {
+    const int h = u / p.pairs_per_head, pr = u - h * p.pairs_per_head;
+    const int w = tile_weight(p, h, 2 * pr) + tile_weight(p, h, 2 * pr + 1);
+    return kSchedBuckets - 1 - min(w, kSchedBuckets - 1);
+}
+
+__global__ void __launch_bounds__(kSchedThreads, 1) bsattn_schedule_kernel(const __grid_constant__ FwdParams p) {
+    grid_launch_dependents();
+    extern __shared__ int run_at[];  // [kSchedChunks][kSchedBuckets]: count, then start
+    __shared__ int warp_sum[kSchedChunks];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = p.num_units;
+    const int run_len = (n + kSchedChunks - 1) / kSchedChunks;
+    for (int i = tid; i < kSchedChunks * kSchedBuckets; i += kSchedThreads) run_at[i] = 0;
     if (tid == 0) *p.sched_counter = 0u;
     __syncthreads();
-    for (int u = tid; u < p.num_units; u += blockDim.x) {
-        const int h = u / p.pairs_per_head, pr = u - h * p.pairs_per_head;
-        const int w = tile_weight(p, h, 2 * pr) + tile_weight(p, h, 2 * pr + 1);
-        const int key = kSchedBuckets - 1 - min(w, kSchedBuckets - 1);
-        key_of[u] = (uint16_t)key;
-        atomicAdd(&start[key], 1);
+    for (int u = tid; u < n; u += kSchedThreads)
+        atomicAdd(&run_at[(u / run_len) * kSchedBuckets + unit_key(p, u)], 1);
+    __syncthreads();
+    // Thread k owns key k: its total over the runs, scanned across keys.
+    const int k = tid;
+    int total = 0;
+#pragma unroll 8
+    for (int c = 0; c < kSchedChunks; ++c) total += run_at[c * kSchedBuckets + k];
+    int incl = total;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int v = warp_sum[lane];
+        int x = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, x, d);
+            if (lane >= d) x += o;
+        }
+        warp_sum[lane] = x - v;
     }
     __syncthreads();
-    if (tid < 32) {  // exclusive scan of the key histogram
-        int running = 0;
-        for (int base = 0; base < kSchedBuckets; base += 32) {
-            const int v = start[base + tid];
-            int incl = v;
-            for (int d = 1; d < 32; d <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, d);
-                if (tid >= d) incl += o;
-            }
-            start[base + tid] = running + incl - v;
-            running += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        // stable scatter, 32 units at a time in unit order
-        const unsigned lt = (1u << tid) - 1u;
-        for (int base = 0; base < p.num_units; base += 32) {
-            const int u = base + tid;
-            const int key = u < p.num_units ? (int)key_of[u] : 0xFFFF;
-            const unsigned peers = __match_any_sync(0xffffffffu, key);
-            if (u < p.num_units) {
-                p.sched_order[start[key] + __popc(peers & lt)] = u;
-            }
-            __syncwarp();
-            if (u < p.num_units && tid == __ffs(peers) - 1) start[key] += __popc(peers);
-            __syncwarp();
-        }
+    int at = warp_sum[warp] + incl - total;  // first position of key k
+#pragma unroll 8
+    for (int c = 0; c < kSchedChunks; ++c) {
+        const int v = run_at[c * kSchedBuckets + k];
+        run_at[c * kSchedBuckets + k] = at;
+        at += v;
     }
+    __syncthreads();
+    // Warp w scatters run w, 32 units at a time in unit order.
+    int *start = run_at + warp * kSchedBuckets;
+    const unsigned lt = (1u << lane) - 1u;
+    const int u_end = min(n, (warp + 1) * run_len);
+    for (int base = warp * run_len; base < u_end; base += 32) {
+        const int u = base + lane;
+        const int key = u < u_end ? unit_key(p, u) : 0xFFFF;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (u < u_end) p.sched_order[start[key] + __popc(peers & lt)] = u;
+        __syncwarp();
+        if (u < u_end && lane == __ffs(peers) - 1) start[key] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+cudaError_t prepare_schedule_kernel() {
+    static int attr_set_for_device[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set_for_device[dev]) {
+        e = cudaFuncSetAttribute(bsattn_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSchedSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set_for_device[dev] = 1;
+    }
+    return cudaSuccess;
 }
 
 template <int D, bool kProxy, bool kPolled, bool kBlocks>
@@ -1284,9 +1335,19 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, const CUtensorMap &tq, const C
                               int grid, cudaStream_t stream) {
     cudaError_t e = prepare_fwd_kernel<D, kProxy, kPolled, kBlocks>();
     if (e != cudaSuccess) return e;
-    bsattn_fwd_kernel<D, kProxy, kPolled, kBlocks>
-        <<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(p, tq, tk, tv, tks, tvs);
-    return cudaGetLastError();
+    // After the scheduling pass the kernel is a programmatic dependent: its CTAs
+    // set up shared memory and TMEM while the pass runs, then wait for it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.dynamic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, bsattn_fwd_kernel<D, kProxy, kPolled, kBlocks>, p, tq, tk, tv, tks, tvs);
 }
 
 template <int D>
@@ -1296,13 +1357,9 @@ cudaError_t launch_fwd_d(const FwdParams &p, const CUtensorMap &tq, const CUtens
     if (p.num_units <= 0) return cudaSuccess;
     cudaError_t e;
     if (p.dynamic) {
-        const size_t key_bytes = (size_t)p.num_units * sizeof(uint16_t);
-        if (key_bytes > 48 * 1024) {
-            e = cudaFuncSetAttribute(bsattn_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)key_bytes);
-            if (e != cudaSuccess) return e;
-        }
-        bsattn_schedule_kernel<<<1, 1024, key_bytes, stream>>>(p);
+        e = prepare_schedule_kernel();
+        if (e != cudaSuccess) return e;
+        bsattn_schedule_kernel<<<1, kSchedThreads, kSchedSmemBytes, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

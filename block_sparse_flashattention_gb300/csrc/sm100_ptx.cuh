@@ -144,6 +144,21 @@ __device__ __forceinline__ void regs_claim() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// -------------------------------------------------- dependent launches --
+
+// Programmatic dependent launch: the grid launched after this one on the stream
+// may start (its CTAs then run up to their dependency wait).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every grid this one depends on has completed and its memory
+// operations are visible; returns at once in a grid launched without the
+// programmatic-serialisation attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
