@@ -28,7 +28,7 @@ TILE = 128
 
 __all__ = ["bsattn_bwd", "bsattn_bwd_workspace_size", "backward", "bsattn_fwd_proxy", "bsattn_kv_summaries", "bsattn_build_meta", "bsattn_build_meta_bitmask", "bsattn_build_meta_blocks", "bsattn_build_meta_bsr", "bsattn_fwd", "bsattn_fwd_static_scratch", "bsattn_fwd_workspace_size", "bsattn_abi_version", "bsattn_testing_set_wait_limit",
            "alloc_meta", "alloc_workspace", "build_meta",
-           "forward", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
+           "forward", "block_sparse_attention", "Meta", "MaskParams", "BsattnError", "status_string", "library", "TILE",
            "OUT_BF16", "OUT_F32", "MASK_NONE", "MASK_CAUSAL", "MASK_SLIDING_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX",
            "BSATTN_OK", "BSATTN_ERR_INVALID_ARG", "BSATTN_ERR_UNSUPPORTED", "BSATTN_ERR_CUDA", "BSATTN_ERR_CAPACITY", "BSATTN_STATIC_SCRATCH_UNITS",
            "FLAG_BAD_COUNT", "FLAG_BAD_INDEX", "FLAG_TIMEOUT", "FLAG_BAD_SEQLENS"]
@@ -167,3 +167,47 @@ def backward(q, k, v, out, lse, dout, meta: Meta, *, cu_seqlens_q=None, cu_seqle
                       gd, workspace, err_flag=err_flag, stream=stream),
            "bsattn_bwd")
     return dq, dk, dv
+
+
+_attention_fn = None
+
+
+def _attention_function():
+    """The autograd Function behind ``block_sparse_attention`` (built on first use,
+    so that importing the package does not import torch)."""
+    global _attention_fn
+    if _attention_fn is None:
+        import torch
+
+        class BlockSparseAttention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, meta, opts):
+                out, lse = forward(q, k, v, meta, **opts)
+                ctx.save_for_backward(q, k, v, out, lse)
+                ctx.meta, ctx.opts = meta, opts
+                return out
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v, out, lse = ctx.saved_tensors
+                dq, dk, dv = backward(q, k, v, out, lse, dout.to(q.dtype).contiguous(), ctx.meta,
+                                      grad_dtype=q.dtype, **ctx.opts)
+                return dq, dk, dv, None, None
+
+        _attention_fn = BlockSparseAttention
+    return _attention_fn
+
+
+def block_sparse_attention(q, k, v, meta: Meta, *, cu_seqlens_q=None, cu_seqlens_k=None,
+                           kv_valid_len=None, kind: int = MASK_NONE,
+                           mask_params: Optional[MaskParams] = None,
+                           softmax_scale: Optional[float] = None, err_flag=None, stream=None):
+    """Differentiable block-sparse attention: ``forward`` with the bf16 output,
+    and on the way back ``backward`` for the incoming gradient of the output
+    (dq, dk, dv in bf16, like q/k/v).  Arguments as for ``forward``; the
+    metadata, sequence offsets, valid lengths and mask parameters are taken as
+    constants (no gradient)."""
+    opts = dict(cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, kv_valid_len=kv_valid_len,
+                kind=kind, mask_params=mask_params, softmax_scale=softmax_scale,
+                err_flag=err_flag, stream=stream)
+    return _attention_function().apply(q, k, v, meta, opts)
