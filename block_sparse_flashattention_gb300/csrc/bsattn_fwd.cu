@@ -297,18 +297,23 @@ __device__ __forceinline__ void softmax_role(const FwdParams &p, const uint32_t 
                 if (ct >= 0 && ct < kTile) c_tail = ct;
             }
             uint32_t s_tail_bits = 0u;
+            float hm0, hm1, hm2, hm3;  // maxima of the four 32-column groups, as loaded
             {
                 uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld32(lane_addr + s_col + 0, v0);
-                tmem_ld32(lane_addr + s_col + 32, v1);
-                tmem_ld32(lane_addr + s_col + 64, v2);
-                tmem_ld32(lane_addr + s_col + 96, v3);
+                tmem_ld32_max(lane_addr + s_col + 0, v0, hm0);
+                tmem_ld32_max(lane_addr + s_col + 32, v1, hm1);
+                tmem_ld32_max(lane_addr + s_col + 64, v2, hm2);
+                tmem_ld32_max(lane_addr + s_col + 96, v3, hm3);
                 if (c_tail >= 0) tmem_ld1(lane_addr + s_col + (uint32_t)c_tail, s_tail_bits);
                 tmem_wait_ld();
                 reg_fence(v0);
                 reg_fence(v1);
                 reg_fence(v2);
                 reg_fence(v3);
+                reg_fence(hm0);
+                reg_fence(hm1);
+                reg_fence(hm2);
+                reg_fence(hm3);
 #pragma unroll
                 for (int x = 0; x < 32; ++x) {
                     s[x] = __uint_as_float(v0[x]);
@@ -318,7 +323,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams &p, const uint32_t 
                 }
             }
             bool tail_kept = false;
-            if (si.flags & (kSMask | kSBound | (kProxy ? kSSummary : 0u))) {
+            const bool masked = (si.flags & (kSMask | kSBound | (kProxy ? kSSummary : 0u))) != 0;
+            if (masked) {
                 // Keep-mask of the 128 columns as four 32-bit words; columns at or
                 // past si.lim (sequence end, valid length) are always dropped.
                 const int j0 = si.n * kTile;
@@ -377,20 +383,18 @@ __device__ __forceinline__ void softmax_role(const FwdParams &p, const uint32_t 
 #pragma unroll
                     for (int x = 0; x < 32; ++x)
                         if (!((keep[w] >> x) & 1u)) s[32 * w + x] = -INFINITY;
+                    // this group's maximum over its kept scores (the load's covers all 32)
+                    float g = fmax3(s[32 * w], s[32 * w + 1], s[32 * w + 2]);
+#pragma unroll
+                    for (int x = 3; x < 31; x += 2) g = fmax3(g, s[32 * w + x], s[32 * w + x + 1]);
+                    g = fmaxf(g, s[32 * w + 31]);
+                    if (w == 0) hm0 = g;
+                    else if (w == 1) hm1 = g;
+                    else if (w == 2) hm2 = g;
+                    else hm3 = g;
                 }
             }
-            float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-            float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-            for (int c = 12; c < 124; c += 8) {
-                mx0 = fmax3(mx0, s[c], s[c + 1]);
-                mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-                mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-                mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-            }
-            mx0 = fmax3(mx0, s[124], s[125]);
-            mx1 = fmax3(mx1, s[126], s[127]);
-            const float m_new = fmaxf(m_run, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
+            const float m_new = fmaxf(m_run, fmax3(hm0, hm1, fmaxf(hm2, hm3)) * sl2);
             // Rescale O only when some row's running maximum grew by more than 2^8;
             // otherwise keep the stale maximum (O / l at the end is the same).
             const bool rescale = (j > 0) && __any_sync(0xffffffffu, (m_new - m_run) > 8.0f);
