@@ -34,6 +34,8 @@
 // num_n(b) entries in either order).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "bsattn_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -331,10 +333,10 @@ __global__ void __launch_bounds__(1024) bsattn_bwd_order_kernel(BwdParams p) {
 
 // ------------------------------------------------------------ 2. row pass --
 // One warp per 4 padded query rows (Q tile, r .. r + 3): D = sum_d dO O in fp32
-// and LSE * log2(e).  Each lane takes D / 32 consecutive elements of every row
+// and LSE * log2(e), both stored negated.  Each lane takes D / 32 consecutive elements of every row
 // (one 8- or 4-byte load of dO and one of O per row), the four rows' loads issued
 // before any is used.  Rows past the sequence, and rows with no keys
-// (LSE = -inf), get LSE2 = +inf, so every probability they would form is 0.
+// (LSE = -inf), get LSE2 = +inf (-inf stored), so every probability they would form is 0.
 constexpr int kRowsPerWarp = 4;
 __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
     const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -396,8 +398,8 @@ __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
             l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
         }
         const long long at = vec_at(p, s, b, h, m) + r0 + lane;
-        p.dvec[at] = dk;
-        p.lse2[at] = l2;
+        p.dvec[at] = -dk;  // negated: the gradient kernels form s log2(e) - LSE2 and dP - D as sums
+        p.lse2[at] = -l2;
     }
 }
 
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             const bool doc = msk && row_on && p.kind == BSATTN_MASK_DOCUMENT;
             const int32_t dk = doc ? p.doc_k[sg.k0 + j] : 0;
-            const float *l2 = vecs + s * 256, *dd = l2 + 128;
+            const float *nl2 = vecs + s * 256, *ndd = nl2 + 128;  // -LSE2, -D of the stage's queries
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(half ? C::bSR2 : C::bSR), it & 1, abort_flag,
@@ -719,19 +721,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
                 uint32_t pw[16], dw[16];
+                // P = 2^(s log2(e) scale - LSE2), dS = P (dP - D), two columns per
+                // packed instruction; dropped columns enter the exponential as -inf.
+                // A chunk every lane keeps whole takes the form without selects.
+                auto form = [&](auto masked) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int c0 = 32 * c + 2 * x;
-                    const float p0 = ((keep >> (2 * x)) & 1u)
-                                         ? ex2_approx(fmaf(__uint_as_float(vs[2 * x]), sl2, -l2[c0])) : 0.f;
-                    const float p1 = ((keep >> (2 * x + 1)) & 1u)
-                                         ? ex2_approx(fmaf(__uint_as_float(vs[2 * x + 1]), sl2, -l2[c0 + 1]))
-                                         : 0.f;
-                    const float ds0 = p0 * (__uint_as_float(vp[2 * x]) - dd[c0]);
-                    const float ds1 = p1 * (__uint_as_float(vp[2 * x + 1]) - dd[c0 + 1]);
-                    pw[x] = pack_bf16x2(p0, p1);
-                    dw[x] = pack_bf16x2(ds0, ds1);
-                }
+                    for (int x = 0; x < 16; ++x) {
+                        const int c0 = 32 * c + 2 * x;
+                        const float2 nl = *reinterpret_cast<const float2 *>(nl2 + c0);
+                        const float2 nd = *reinterpret_cast<const float2 *>(ndd + c0);
+                        float x0, x1, t0, t1, d0, d1;
+                        ffma2(x0, x1, __uint_as_float(vs[2 * x]), __uint_as_float(vs[2 * x + 1]), sl2, sl2,
+                              nl.x, nl.y);
+                        if constexpr (decltype(masked)::value) {
+                            x0 = ((keep >> (2 * x)) & 1u) ? x0 : -INFINITY;
+                            x1 = ((keep >> (2 * x + 1)) & 1u) ? x1 : -INFINITY;
+                        }
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        fadd2(t0, t1, __uint_as_float(vp[2 * x]), __uint_as_float(vp[2 * x + 1]), nd.x, nd.y);
+                        fmul2(d0, d1, p0, p1, t0, t1);
+                        pw[x] = pack_bf16x2(p0, p1);
+                        dw[x] = pack_bf16x2(d0, d1);
+                    }
+                };
+                if (__all_sync(0xffffffffu, keep == 0xffffffffu)) form(std::false_type{});
+                else form(std::true_type{});
                 tmem_st16(tS + la + 32u * c, pw);
                 tmem_st16(tP + la + 32u * c, dw);
                 tmem_wait_st();
@@ -987,7 +1001,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t la = (q4 * 32u) << 16;
         const int i = m * kTile + r;           // sequence-local query
         const long long vrow = vec_at(p, sg, b, h, m) + r;
-        const float l2 = p.lse2[vrow], dd = p.dvec[vrow];
+        const float nl2 = p.lse2[vrow], ndd = p.dvec[vrow];  // -LSE2, -D of this query row
         const float sl2 = p.scale_log2;
         const int32_t dqid = (p.kind == BSATTN_MASK_DOCUMENT && i < sg.sq) ? p.doc_q[sg.q0 + i] : 0;
         bool ok = true;
@@ -1040,13 +1054,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
                 uint32_t dw[16];
+                // dS = 2^(s log2(e) scale - LSE2) (dP - D), two columns per packed
+                // instruction; dropped columns enter the exponential as -inf.  A
+                // chunk every lane keeps whole takes the form without selects.
+                auto form = [&](auto masked) {
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const float p0 = ((keep >> (2 * x)) & 1u) ? ex2_approx(fmaf(__uint_as_float(vs[2 * x]), sl2, -l2)) : 0.f;
-                    const float p1 =
-                        ((keep >> (2 * x + 1)) & 1u) ? ex2_approx(fmaf(__uint_as_float(vs[2 * x + 1]), sl2, -l2)) : 0.f;
-                    dw[x] = pack_bf16x2(p0 * (__uint_as_float(vp[2 * x]) - dd), p1 * (__uint_as_float(vp[2 * x + 1]) - dd));
-                }
+                    for (int x = 0; x < 16; ++x) {
+                        float x0, x1, t0, t1, d0, d1;
+                        ffma2(x0, x1, __uint_as_float(vs[2 * x]), __uint_as_float(vs[2 * x + 1]), sl2, sl2, nl2,
+                              nl2);
+                        if constexpr (decltype(masked)::value) {
+                            x0 = ((keep >> (2 * x)) & 1u) ? x0 : -INFINITY;
+                            x1 = ((keep >> (2 * x + 1)) & 1u) ? x1 : -INFINITY;
+                        }
+                        fadd2(t0, t1, __uint_as_float(vp[2 * x]), __uint_as_float(vp[2 * x + 1]), ndd, ndd);
+                        fmul2(d0, d1, ex2_approx(x0), ex2_approx(x1), t0, t1);
+                        dw[x] = pack_bf16x2(d0, d1);
+                    }
+                };
+                if (__all_sync(0xffffffffu, keep == 0xffffffffu)) form(std::false_type{});
+                else form(std::true_type{});
                 tmem_st16(tDS + 64u * s + la + 16u * c, dw);
                 tmem_wait_st();
                 tc_fence_before();

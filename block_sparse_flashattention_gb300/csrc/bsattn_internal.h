@@ -116,7 +116,8 @@ struct BwdParams {
     int o_f32;
     const uint16_t *dout;         // bf16, layout of q
     const float *lse;             // batched [B, H, S_q], varlen [H, rows_q]; natural log
-    float *lse2, *dvec;           // workspace, 128 rows per Q tile: LSE * log2(e), D
+    float *lse2, *dvec;           // workspace, 128 rows per Q tile: -LSE * log2(e), -D (negated:
+                                  // the gradient kernels add them)
     void *dq, *dk, *dv;           // gradients in q / k / v layouts
     int grad_f32;
     int32_t *err;
