@@ -788,9 +788,10 @@ struct DqCfg {
     static constexpr uint32_t kV = kK + kKStages * kTileBytes;   // V stage s at kV + s * kTileBytes
     static constexpr uint32_t kBar = kV + kVStages * kTileBytes;
     // barriers: resident tiles, K full [3], K empty [3], V full [2], V empty [2],
-    // S and dP ready (two halves), dS done (two halves), dQ done, MMA drain
-    static constexpr int bRF = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSR = 11, bSR2 = 12, bPR = 13;
-    static constexpr int bPR2 = 14, bDone = 15, bDrain = 16, kNumBars = 17;
+    // S and dP ready, S and dP in the elementwise warps' registers [2: even and
+    // odd items], dS done [2: even and odd items], dQ done, MMA drain
+    static constexpr int bRF = 0, bKF = 1, bKE = 4, bVF = 7, bVE = 9, bSR = 11, bSL = 12, bPR = 14;
+    static constexpr int bDone = 16, bDrain = 17, kNumBars = 18;
     static constexpr uint32_t kInfo = kBar + kNumBars * 8;       // int32 [3][2]: tile, mask flag
     static constexpr uint32_t kMisc = kInfo + 32;                // [0] tmem base, [1] abort
     static constexpr uint32_t kBytes = kMisc + 16;
@@ -813,9 +814,10 @@ __device__ __forceinline__ void dq_init(uint8_t *gbase, uint32_t base, uint32_t 
             mbar_init(bar(C::bVE + s), 1);
         }
         mbar_init(bar(C::bSR), 1);
-        mbar_init(bar(C::bSR2), 1);
-        mbar_init(bar(C::bPR), kEwWarps);
-        mbar_init(bar(C::bPR2), kEwWarps);
+        for (int e = 0; e < 2; ++e) {
+            mbar_init(bar(C::bSL + e), kEwWarps);
+            mbar_init(bar(C::bPR + e), kEwWarps);
+        }
         mbar_init(bar(C::bDone), 1);
         mbar_init(bar(C::bDrain), 1);
         misc[1] = 0;
@@ -838,10 +840,10 @@ __device__ __forceinline__ void dq_init(uint8_t *gbase, uint32_t base, uint32_t 
 // pass through the K and V rings.  Thread = query row; column group cg of the
 // elementwise warps takes key chunk 2 h + cg of key half h.
 // TMEM: S [0, 128), dP [128, 256), dS buffers (bf16) [256, 320) and [320, 384),
-// dQ [384, 384 + D).  S and dP are formed in two key halves; half h of tile t + 1
-// is issued as soon as the elementwise warps have finished half h of tile t,
-// before that half's dQ product, which reads dS buffer t % 2 while the
-// elementwise warps fill the other one.
+// dQ [384, 384 + D).  S and dP are full-width (N = 128) products; those of tile
+// t + 1 are issued as soon as the elementwise warps hold tile t's in registers,
+// so they run under tile t's elementwise work, ahead of tile t's dQ product,
+// which reads dS buffer t % 2 while the elementwise warps fill the other one.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dq_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
@@ -927,68 +929,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // PR_h of tile t: dQ += dS_h K_h of tile t, then half h of tile t + 1 (its
         // first half waits for K and then V of tile t + 1, so the dQ product runs
         // while they land).
-        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 64, false);
+        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
         constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dQk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dOk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        // S_h = Q K_h^T (rows 64 h.. of the item's K stage), or dP_h = dO V_h^T
-        auto issue_mm = [&](int it, int half, bool dp) {
+        // S = Q K^T over the 128 keys of the item's K stage, or dP = dO V^T
+        auto issue_mm = [&](int it, bool dp) {
             const uint32_t st = base + (dp ? C::kV + (uint32_t)(it % C::kVStages) * C::kTileBytes
-                                           : C::kK + (uint32_t)(it % C::kKStages) * C::kTileBytes) +
-                                (uint32_t)half * 8192u;
+                                           : C::kK + (uint32_t)(it % C::kKStages) * C::kTileBytes);
             const uint64_t dB = smem_desc_sw128(st, 16, 1024);
             const uint64_t dA = dp ? dOk : dQk;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, (dp ? tP : tS) + 64u * half, dA + off, dB + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, dp ? tP : tS, dA + off, dB + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_dq = [&](int it, int half) {  // dQ += dS_h K_h (16 keys per step)
+        auto issue_dq = [&](int it) {  // dQ += dS K (16 keys per step)
             const uint64_t dKm =
                 smem_desc_sw128(base + C::kK + (uint32_t)(it % C::kKStages) * C::kTileBytes, C::kSubBytes, 1024);
 #pragma unroll
-            for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
+            for (int kk = 0; kk < 8; ++kk)
                 mma_ts_lead(lead, tdQ, tDS + 64u * (uint32_t)(it & 1) + 8u * kk, dKm + (uint64_t)(kk * (2048 >> 4)),
                             idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
         };
-        // first half of item it: S after its K lands, dP after its V lands
-        auto first_half = [&](int it) -> bool {
+        // S of item it after its K lands, dP after its V lands; the V stage is
+        // free once dP has read it
+        auto issue_s = [&](int it) -> bool {
             if (!mbar_wait(bar(C::bKF + it % C::kKStages), (it / C::kKStages) & 1, abort_flag, p.err,
                            BSATTN_FLAG_TIMEOUT))
                 return false;
             tc_fence_after();
-            issue_mm(it, 0, false);
+            issue_mm(it, false);
             if (!mbar_wait(bar(C::bVF + it % C::kVStages), (it / C::kVStages) & 1, abort_flag, p.err,
                            BSATTN_FLAG_TIMEOUT))
                 return false;
             tc_fence_after();
-            issue_mm(it, 0, true);
+            issue_mm(it, true);
             mma_commit_lead(lead, bar(C::bSR));
-            return true;
-        };
-        // second half of item it; its V stage is free once these have read it
-        auto second_half = [&](int it) {
-            issue_mm(it, 1, false);
-            issue_mm(it, 1, true);
-            mma_commit_lead(lead, bar(C::bSR2));
             mma_commit_lead(lead, bar(C::bVE + it % C::kVStages));
+            return true;
         };
         bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
         tc_fence_after();
-        if (ok && total > 0 && (ok = first_half(0))) second_half(0);
+        if (ok && total > 0) ok = issue_s(0);
         for (int it = 0; ok && it < total; ++it) {
-            const bool more = it + 1 < total;
-            if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
+            if (it + 1 < total) {
+                // S and dP of this item are in the elementwise warps' registers
+                if (!(ok = mbar_wait(bar(C::bSL + (it & 1)), (it >> 1) & 1, abort_flag, p.err,
+                                     BSATTN_FLAG_TIMEOUT)))
+                    break;
+                tc_fence_after();
+                if (!(ok = issue_s(it + 1))) break;
+            }
+            if (!(ok = mbar_wait(bar(C::bPR + (it & 1)), (it >> 1) & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)))
+                break;
             tc_fence_after();
-            issue_dq(it, 0);
-            if (more && !(ok = first_half(it + 1))) break;
-            if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
-            if (more) second_half(it + 1);
-            issue_dq(it, 1);
-            mma_commit_lead(lead, bar(C::bKE + it % C::kKStages));  // K stage free once these have read it
+            issue_dq(it);
+            mma_commit_lead(lead, bar(C::bKE + it % C::kKStages));  // K stage free once dQ has read it
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
         mma_commit_lead(lead, bar(C::bDrain));
@@ -1030,19 +1029,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
             const bool doc = msk && p.kind == BSATTN_MASK_DOCUMENT;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bSR), it & 1, abort_flag, p.err,
+                                                         BSATTN_FLAG_TIMEOUT))))
+                break;
+            tc_fence_after();
+            // key chunks cg and cg + 2 (32 columns each) of S and dP, one after the
+            // other; once the second is in registers the MMA warp may overwrite both
+            uint32_t dw[2][16];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(half ? C::bSR2 : C::bSR), it & 1, abort_flag,
-                                                             p.err, BSATTN_FLAG_TIMEOUT))))
-                    break;
-                tc_fence_after();
-                const int c = 2 * half + cg;  // key chunk: columns [32 c, 32 c + 32)
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int c = cg + 2 * k2;  // key chunk: columns [32 c, 32 c + 32)
                 uint32_t vs[32], vp[32];
                 tmem_ld32(tS + la + 32u * c, vs);
                 tmem_ld32(tP + la + 32u * c, vp);
                 tmem_wait_ld();
                 reg_fence(vs);
                 reg_fence(vp);
+                if (k2 == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::bSL + s));
+                }
                 uint32_t keep = bwd_span_bits(lo0 - 32 * c, hi0 - 32 * c) | bwd_span_bits(lo1 - 32 * c, hi1 - 32 * c);
                 if (doc) {
                     keep = 0u;
@@ -1053,7 +1060,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             keep |= 1u << x;
                     }
                 }
-                uint32_t dw[16];
                 // dS = 2^(s log2(e) scale - LSE2) (dP - D), two columns per packed
                 // instruction; dropped columns enter the exponential as -inf.  A
                 // chunk every lane keeps whole takes the form without selects.
@@ -1069,18 +1075,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         }
                         fadd2(t0, t1, __uint_as_float(vp[2 * x]), __uint_as_float(vp[2 * x + 1]), ndd, ndd);
                         fmul2(d0, d1, ex2_approx(x0), ex2_approx(x1), t0, t1);
-                        dw[x] = pack_bf16x2(d0, d1);
+                        dw[k2][x] = pack_bf16x2(d0, d1);
                     }
                 };
                 if (__all_sync(0xffffffffu, keep == 0xffffffffu)) form(std::false_type{});
                 else form(std::true_type{});
-                tmem_st16(tDS + 64u * s + la + 16u * c, dw);
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(half ? C::bPR2 : C::bPR));
             }
-            if (!ok) break;
+            tmem_st16(tDS + 64u * s + la + 16u * cg, dw[0]);
+            tmem_st16(tDS + 64u * s + la + 16u * (cg + 2), dw[1]);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::bPR + s));
         }
         // ------------------------------------------------- epilogue --
         if (ok && total > 0) {
