@@ -1033,23 +1033,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                          BSATTN_FLAG_TIMEOUT))))
                 break;
             tc_fence_after();
-            // key chunks cg and cg + 2 (32 columns each) of S and dP, one after the
-            // other; once the second is in registers the MMA warp may overwrite both
+            // key chunks cg and cg + 2 (32 columns each) of S and dP; once both are
+            // in registers the MMA warp may overwrite them with the next tile's
             uint32_t dw[2][16];
+            uint32_t vsa[2][32], vpa[2][32];
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                tmem_ld32(tS + la + 32u * (cg + 2 * k2), vsa[k2]);
+                tmem_ld32(tP + la + 32u * (cg + 2 * k2), vpa[k2]);
+            }
+            tmem_wait_ld();
+            reg_fence(vsa[0]);
+            reg_fence(vpa[0]);
+            reg_fence(vsa[1]);
+            reg_fence(vpa[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::bSL + s));
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
                 const int c = cg + 2 * k2;  // key chunk: columns [32 c, 32 c + 32)
-                uint32_t vs[32], vp[32];
-                tmem_ld32(tS + la + 32u * c, vs);
-                tmem_ld32(tP + la + 32u * c, vp);
-                tmem_wait_ld();
-                reg_fence(vs);
-                reg_fence(vp);
-                if (k2 == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::bSL + s));
-                }
+                const uint32_t (&vs)[32] = vsa[k2];
+                const uint32_t (&vp)[32] = vpa[k2];
                 uint32_t keep = bwd_span_bits(lo0 - 32 * c, hi0 - 32 * c) | bwd_span_bits(lo1 - 32 * c, hi1 - 32 * c);
                 if (doc) {
                     keep = 0u;
