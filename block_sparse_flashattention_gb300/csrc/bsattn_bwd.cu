@@ -13,15 +13,19 @@
 //      KV-major full / mask lists, Q tiles in descending order;
 //   2. an order pass: KV tiles sorted by list length, longest first, so the
 //      dK / dV grid starts its longest CTAs first;
-//   3. a row pass writing D and LSE * log2(e) into rows padded to 128 per Q tile;
+//   3. a row pass writing -D and -LSE * log2(e) into rows padded to 128 per Q
+//      tile (negated, so that the gradient kernels add them);
 //   4. the dK / dV kernel: one CTA per KV tile, S^T = K Q^T and dP^T = V dO^T per
 //      listed Q tile on tcgen05 in two query halves, P^T and dS^T formed per key
 //      row in TMEM, dV += P^T dO and dK += dS^T Q accumulated in TMEM; half h of
 //      the next Q tile is issued as soon as this one's half h is done, so the
 //      products of one half overlap the elementwise work of the other;
 //   5. the dQ kernel: one CTA per Q tile, S = Q K^T and dP = dO V^T per listed KV
-//      tile in two key halves, dS per query row into one of two TMEM buffers,
-//      dQ += dS K accumulated in TMEM, pipelined the same way.
+//      tile as full-width products, dS per query row into one of two TMEM
+//      buffers, dQ += dS K accumulated in TMEM; the next KV tile's S and dP are
+//      issued once this tile's are in the elementwise warps' registers.
+// Both elementwise passes form P and dS two columns per packed f32x2
+// instruction, a dropped column entering the exponential as -inf.
 // P is recomputed from the forward's LSE (no running maximum) and rounded to
 // bf16 before the P^T dO product, as the forward rounds it before P V; dS is
 // rounded to bf16 before its products.
