@@ -520,6 +520,18 @@ def oracle_timing(cpu_seconds):
     return res
 
 
+def workload_config(wl, blocks, ws):
+    """The `config` object of both arms: the workload, its computed tiles and FLOP."""
+    import numpy as np
+    q_bytes = 2 * int(np.prod(wl.q_shape()))
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "S": int(wl.seqlens_q[0]), "D": wl.D,
+            "tile": "128x128", "computed_tiles": int(blocks),
+            "flop_per_step": int(blocks) * flop_per_tile(wl.D),
+            "step": "metadata kernel + attention kernel",
+            "l2": "inputs larger than L2 (Q/K/V %.2f GB vs 129 MB)" % (3 * q_bytes / 1e9),
+            "parallelism": f"replicas x{ws}"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -529,6 +541,8 @@ def run_reference(args):
     from workloads import make_workload
     wl = make_workload(args.config)
     q, k, v = wl.qkv()
+    ref_meta = oracle.build_meta(wl)
+    blocks = int(ref_meta["full_cnt"].sum() + ref_meta["mask_cnt"].sum())
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(wl, q, k, v, per_step)
@@ -545,8 +559,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": wall * 1e3 / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "S": int(wl.seqlens_q[0]),
-                       "D": wl.D},
+            "config": workload_config(wl, blocks, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -765,13 +778,7 @@ def run_native(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "S": sq, "D": wl.D,
-                   "tile": "128x128", "computed_tiles": blocks,
-                   "flop_per_step": flop_step,
-                   "step": "metadata kernel + attention kernel",
-                   "l2": "inputs larger than L2 (Q/K/V %.2f GB vs 129 MB)" % (
-                       3 * hq.numel() * 2 / 1e9),
-                   "parallelism": f"replicas x{ws}"},
+        "config": workload_config(wl, blocks, ws),
         "fwd_ms": fwd_mean, "meta_ms": statistics.mean(meta_ms),
         "fwd_tflops": achieved, "frac_of_peak_step": value / ws / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
