@@ -407,25 +407,30 @@ __global__ void __launch_bounds__(256) bsattn_bwd_rows_kernel(BwdParams p) {
     }
 }
 
-// Shared memory of both gradient kernels: two resident tiles, a ring of two
-// stages of two tiles plus two 128-float vectors, barriers, item info, misc.
+// Shared memory of the dK/dV kernel: K and V resident, a ring of Q tiles (each
+// with its queries' -LSE2 and -D vectors) and a ring of dO tiles, barriers,
+// item info, misc.  dO leaves the ring after the dV product, Q after the dK
+// product, one product later.
 template <int D>
 struct BwdCfg {
     static constexpr uint32_t kTileBytes = kTile * D * 2;
     static constexpr int kSub = D / 64;                       // 64-column swizzle spans per tile
     static constexpr uint32_t kSubBytes = kTile * 64 * 2;
-    static constexpr uint32_t kRes0 = 0, kRes1 = kTileBytes;  // resident tiles
-    static constexpr uint32_t kSt = 2 * kTileBytes;           // stage s: kSt + s * 2 * kTileBytes
-    static constexpr uint32_t kVec = kSt + 4 * kTileBytes;   // stage s: 2 x 128 floats at kVec + 1024 s
-    static constexpr uint32_t kBar = kVec + 2048;
-    // barriers: resident tiles full, stage full [2] (dQ kernel: its first tile,
-    // K), stage second tile full [2] (dQ kernel: V), stage empty [2], S and dP
-    // ready (first / second half of the tile), elementwise done (first / second
-    // half), accumulators done, MMA drain
-    static constexpr int bRF = 0, bF = 1, bF2 = 3, bE = 5, bSR = 7, bSR2 = 8, bPR = 9, bPR2 = 10;
-    static constexpr int bDone = 11, bDrain = 12, kNumBars = 13;
-    static constexpr uint32_t kInfo = kBar + kNumBars * 8;    // int32 [2][4]
-    static constexpr uint32_t kMisc = kInfo + 32;             // [0] tmem base, [1] abort
+    static constexpr int kQStages = 2, kOStages = 2;
+    static constexpr uint32_t kRes0 = 0, kRes1 = kTileBytes;  // K, V
+    static constexpr uint32_t kQ = 2 * kTileBytes;            // Q stage s at kQ + s * kTileBytes
+    static constexpr uint32_t kO = kQ + kQStages * kTileBytes;  // dO stage s at kO + s * kTileBytes
+    static constexpr uint32_t kVec = kO + kOStages * kTileBytes;  // Q stage s: 2 x 128 floats at kVec + 1024 s
+    static constexpr uint32_t kBar = kVec + 1024 * kQStages;
+    // barriers: resident tiles full, Q full / empty [kQStages], dO full / empty
+    // [kOStages], S^T done, dP^T done, P^T written [2: query halves], dP^T in
+    // the elementwise warps' registers, dS^T written [2: query halves],
+    // accumulators done, MMA drain
+    static constexpr int bRF = 0, bQF = 1, bQE = bQF + kQStages, bOF = bQE + kQStages, bOE = bOF + kOStages;
+    static constexpr int bS = bOE + kOStages, bP = bS + 1, bPt = bP + 1, bDL = bPt + 2, bDS = bDL + 1;
+    static constexpr int bDone = bDS + 2, bDrain = bDone + 1, kNumBars = bDrain + 1;
+    static constexpr uint32_t kInfo = kBar + kNumBars * 8;    // int32 [kQStages][2]: Q tile, mask flag
+    static constexpr uint32_t kMisc = kInfo + 8 * kQStages;   // [0] tmem base, [1] abort
     static constexpr uint32_t kBytes = kMisc + 16;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
@@ -448,15 +453,21 @@ __device__ __forceinline__ void bwd_init(uint8_t *gbase, uint32_t base, uint32_t
     auto bar = [&](int i) -> uint32_t { return base + C::kBar + 8u * (uint32_t)i; };
     if (threadIdx.x == 0) {
         mbar_init(bar(C::bRF), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(C::bF + s), 1);
-            mbar_init(bar(C::bF2 + s), 1);
-            mbar_init(bar(C::bE + s), 1);
+        for (int s = 0; s < C::kQStages; ++s) {
+            mbar_init(bar(C::bQF + s), 1);
+            mbar_init(bar(C::bQE + s), 1);
         }
-        mbar_init(bar(C::bSR), 1);
-        mbar_init(bar(C::bSR2), 1);
-        mbar_init(bar(C::bPR), kEwWarps);  // one arrival per elementwise warp
-        mbar_init(bar(C::bPR2), kEwWarps);
+        for (int s = 0; s < C::kOStages; ++s) {
+            mbar_init(bar(C::bOF + s), 1);
+            mbar_init(bar(C::bOE + s), 1);
+        }
+        mbar_init(bar(C::bS), 1);
+        mbar_init(bar(C::bP), 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar(C::bPt + k), kEwWarps);  // one arrival per elementwise warp
+            mbar_init(bar(C::bDS + k), kEwWarps);
+        }
+        mbar_init(bar(C::bDL), kEwWarps);
         mbar_init(bar(C::bDone), 1);
         mbar_init(bar(C::bDrain), 1);
         misc[1] = 0;
@@ -520,20 +531,28 @@ __device__ __forceinline__ void bwd_epilogue_half(uint32_t tacc, bool have, bool
 
 // ----------------------------------------------------------- 4. dK and dV --
 // One CTA per (b, h, KV tile n), taken in the order of the order pass; 384
-// threads: warp 0 loads (K and V of the tile once, then Q, dO, LSE2 and D of
-// each listed Q tile into a two-stage ring), warp 1 issues the MMAs, warp 2 owns
-// TMEM, warps 4-11 form P^T and dS^T (warp w: TMEM lane quarter w % 4, thread =
-// key row; column group (w - 4) / 4 takes query columns [32 cg, 32 cg + 32) of
-// each half) and write the gradients.
-// TMEM: S^T [0, 128), dP^T [128, 256), dV [256, 256 + D), dK [256 + D, 256 + 2D).
-// P^T (bf16) of query chunk c (32 columns) goes to columns [32 c, 32 c + 16) of
-// S^T, inside the chunk's own fp32 columns, and dS^T likewise within dP^T.
+// threads: warp 0 loads (K and V of the tile once, then Q with LSE2 and D, and
+// dO of each listed Q tile into their rings), warp 1 issues the MMAs, warp 2
+// owns TMEM, warps 4-11 form P^T and dS^T (warp w: TMEM lane quarter w % 4,
+// thread = key row; column group cg = (w - 4) / 4 takes query chunks cg and
+// cg + 2, 32 columns each) and write the gradients.
+// TMEM: two 128-column regions R0 = [0, 128), R1 = [128, 256), dV [256, 256 + D),
+// dK [256 + D, 256 + 2D).  Q tile t: S^T (N = 128) in R(t % 2), dP^T in
+// R((t + 1) % 2).  P^T (bf16) of query chunk c goes to columns [32 c, 32 c + 16)
+// of R(t % 2) and dS^T to [32 c + 16, 32 c + 32), inside the chunk's own S^T
+// columns, so dP^T's region is free as soon as the elementwise warps hold it in
+// registers: S^T of tile t + 1 goes there, and dP^T of tile t + 1 into R(t % 2)
+// after tile t's dK product (products run in issue order).  Tensor core order
+// per tile: dV_t, S_t+1, dK_t, dP_t+1, so each product covers the elementwise
+// step the next one waits for (P^T of t + 1 forms under dK_t and dP_t+1, dS^T
+// of t under dV_t and S_t+1).
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bsattn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tq,
                            const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                            const __grid_constant__ CUtensorMap tdo) {
     using C = BwdCfg<D>;
+    constexpr int kQS = C::kQStages, kOS = C::kOStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -556,7 +575,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     bwd_init<D>(gbase, base, warp);
     const uint32_t tmem = misc[0];
-    const uint32_t tS = tmem, tP = tmem + 128u, tdV = tmem + 256u, tdK = tmem + 256u + D;
+    const uint32_t tdV = tmem + 256u, tdK = tmem + 256u + D;
+    auto region = [&](int t) -> uint32_t { return tmem + 128u * (uint32_t)(t & 1); };  // S^T of tile t
 
     if (warp == 0) {
         // ------------------------------------------------------- loads --
@@ -566,99 +586,109 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_3d_lead(lead, base + C::kRes0 + x * C::kSubBytes, &tk, bar(C::bRF), x * 64, h, kvrow);
             tma_load_3d_lead(lead, base + C::kRes1 + x * C::kSubBytes, &tv, bar(C::bRF), x * 64, h, kvrow);
         }
-        int it = 0;
-        for (; it < total; ++it) {
-            const int s = it & 1;
-            if (!mbar_wait(bar(C::bE + s), ((it >> 1) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
+        int nq = 0, no = 0;  // Q and dO tiles issued
+        for (int it = 0; it < total; ++it) {
+            const int qs = it % kQS, os = it % kOS;
+            if (!mbar_wait(bar(C::bQE + qs), ((it / kQS) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
             const int m = it < cm ? p.t_mask_idx[li + it] : p.t_full_idx[li + (it - cm)];
-            info[s * 4 + 0] = m;
-            info[s * 4 + 1] = it < cm ? 1 : 0;
+            info[qs * 2 + 0] = m;
+            info[qs * 2 + 1] = it < cm ? 1 : 0;
             const int qrow = (int)(sg.q0 + m * kTile);
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
-            mbar_arrive_expect_tx_lead(lead, bar(C::bF + s), 2 * C::kTileBytes + 1024u);
-            for (int x = 0; x < C::kSub; ++x) {
-                tma_load_3d_lead(lead, st + x * C::kSubBytes, &tq, bar(C::bF + s), x * 64, h, qrow);
-                tma_load_3d_lead(lead, st + C::kTileBytes + x * C::kSubBytes, &tdo, bar(C::bF + s), x * 64,
-                                 h, qrow);
-            }
             const long long vrow = vec_at(p, sg, b, h, m);
-            bulk_g2s_lead(lead, base + C::kVec + 1024u * s, p.lse2 + vrow, 512u, bar(C::bF + s));
-            bulk_g2s_lead(lead, base + C::kVec + 1024u * s + 512u, p.dvec + vrow, 512u, bar(C::bF + s));
+            mbar_arrive_expect_tx_lead(lead, bar(C::bQF + qs), C::kTileBytes + 1024u);
+            for (int x = 0; x < C::kSub; ++x)
+                tma_load_3d_lead(lead, base + C::kQ + qs * C::kTileBytes + x * C::kSubBytes, &tq, bar(C::bQF + qs),
+                                 x * 64, h, qrow);
+            bulk_g2s_lead(lead, base + C::kVec + 1024u * qs, p.lse2 + vrow, 512u, bar(C::bQF + qs));
+            bulk_g2s_lead(lead, base + C::kVec + 1024u * qs + 512u, p.dvec + vrow, 512u, bar(C::bQF + qs));
+            ++nq;
+            if (!mbar_wait(bar(C::bOE + os), ((it / kOS) & 1) ^ 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT)) break;
+            mbar_arrive_expect_tx_lead(lead, bar(C::bOF + os), C::kTileBytes);
+            for (int x = 0; x < C::kSub; ++x)
+                tma_load_3d_lead(lead, base + C::kO + os * C::kTileBytes + x * C::kSubBytes, &tdo, bar(C::bOF + os),
+                                 x * 64, h, qrow);
+            ++no;
         }
         // every copy issued has landed before the CTA may exit
         mbar_wait_drain(bar(C::bRF), 0);
-        for (int s = 0; s < 2; ++s) {
-            const int uses = (it + 1 - s) / 2;
-            if (uses > 0) mbar_wait_drain(bar(C::bF + s), (uint32_t)(uses - 1) & 1u);
+        for (int s = 0; s < kQS; ++s) {
+            const int uses = (nq + kQS - 1 - s) / kQS;
+            if (uses > 0) mbar_wait_drain(bar(C::bQF + s), (uint32_t)(uses - 1) & 1u);
+        }
+        for (int s = 0; s < kOS; ++s) {
+            const int uses = (no + kOS - 1 - s) / kOS;
+            if (uses > 0) mbar_wait_drain(bar(C::bOF + s), (uint32_t)(uses - 1) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMAs --
-        // Per listed Q tile, in two query halves h (N = 64): S^T_h, dP^T_h -> SR_h;
-        // after PR_h, dV and dK over half h.  Half h of the next tile is issued
-        // right after this tile's half-h gradient products, so the tensor core
-        // works on one half while the elementwise warps work on the other.
-        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 64, false);
+        constexpr uint32_t idesc_ss = idesc_bf16_f32(128, 128, false);
         constexpr uint32_t idesc_ts = idesc_bf16_f32(128, D, true);
         constexpr uint64_t kSubUnits = C::kSubBytes >> 4;
         const uint64_t dKk = smem_desc_sw128(base + C::kRes0, 16, 1024);
         const uint64_t dVk = smem_desc_sw128(base + C::kRes1, 16, 1024);
-        auto issue_s = [&](int s, int half) {  // S^T = K Q_h^T, dP^T = V dO_h^T (rows 64 h.. of the stage)
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes + (uint32_t)half * 8192u;
-            const uint64_t dQk = smem_desc_sw128(st, 16, 1024);
-            const uint64_t dOk = smem_desc_sw128(st + C::kTileBytes, 16, 1024);
+        // S^T = K Q_t^T into region(t), or dP^T = V dO_t^T into region(t + 1)
+        auto issue_mm = [&](int t, bool dp) {
+            const uint32_t st = dp ? base + C::kO + (uint32_t)(t % kOS) * C::kTileBytes
+                                   : base + C::kQ + (uint32_t)(t % kQS) * C::kTileBytes;
+            const uint64_t dB = smem_desc_sw128(st, 16, 1024);
+            const uint64_t dA = dp ? dVk : dKk;
+            const uint32_t td = region(dp ? t + 1 : t);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tS + 64u * half, dKk + off, dQk + off, idesc_ss, kk > 0 ? 1u : 0u);
+                mma_ss_lead(lead, td, dA + off, dB + off, idesc_ss, kk > 0 ? 1u : 0u);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t off = (uint64_t)((kk >> 2) * kSubUnits + (kk & 3) * 2);
-                mma_ss_lead(lead, tP + 64u * half, dVk + off, dOk + off, idesc_ss, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_lead(lead, bar(half ? C::bSR2 : C::bSR));
         };
-        auto issue_grad = [&](int s, int half, int it) {  // dV += P^T_h dO_h, dK += dS^T_h Q_h
-            const uint32_t st = base + C::kSt + (uint32_t)s * 2u * C::kTileBytes;
-            const uint64_t dOm = smem_desc_sw128(st + C::kTileBytes, C::kSubBytes, 1024);
-            const uint64_t dQm = smem_desc_sw128(st, C::kSubBytes, 1024);
-#pragma unroll
-            for (int kk = 4 * half; kk < 4 * half + 4; ++kk)  // 16 queries per step
-                mma_ts_lead(lead, tdV, tS + 32u * (kk >> 1) + 8u * (kk & 1),
-                            dOm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+        // dV += P^T_t dO_t, or dK += dS^T_t Q_t, over query half `half` (16 queries per step)
+        auto issue_grad = [&](int t, bool dk, int half) {
+            const uint32_t st = dk ? base + C::kQ + (uint32_t)(t % kQS) * C::kTileBytes
+                                   : base + C::kO + (uint32_t)(t % kOS) * C::kTileBytes;
+            const uint64_t dBm = smem_desc_sw128(st, C::kSubBytes, 1024);
+            const uint32_t ta = region(t) + (dk ? 16u : 0u);
 #pragma unroll
             for (int kk = 4 * half; kk < 4 * half + 4; ++kk)
-                mma_ts_lead(lead, tdK, tP + 32u * (kk >> 1) + 8u * (kk & 1),
-                            dQm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_lead(lead, dk ? tdK : tdV, ta + 32u * (kk >> 1) + 8u * (kk & 1),
+                            dBm + (uint64_t)(kk * (2048 >> 4)), idesc_ts, (t > 0 || kk > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait(bar(C::bRF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
-        tc_fence_after();
-        if (ok && total > 0) {
-            ok = mbar_wait(bar(C::bF), 0, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
+        auto wait = [&](int bi, int par) -> bool {
+            const bool r = mbar_wait(bar(bi), (uint32_t)par & 1u, abort_flag, p.err, BSATTN_FLAG_TIMEOUT);
             tc_fence_after();
-            if (ok) {
-                issue_s(0, 0);
-                issue_s(0, 1);
+            return r;
+        };
+        bool ok = wait(C::bRF, 0);
+        if (ok && total > 0) {
+            if ((ok = wait(C::bQF, 0))) {
+                issue_mm(0, false);
+                mma_commit_lead(lead, bar(C::bS));
+            }
+            if (ok && (ok = wait(C::bOF, 0))) {
+                issue_mm(0, true);
+                mma_commit_lead(lead, bar(C::bP));
             }
         }
         for (int it = 0; ok && it < total; ++it) {
-            const int s = it & 1;
             const bool more = it + 1 < total;
-            if (!(ok = mbar_wait(bar(C::bPR), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
-            issue_grad(s, 0, it);
+            if (!(ok = wait(C::bPt, it))) break;
+            issue_grad(it, false, 0);
+            if (!(ok = wait(C::bPt + 1, it))) break;
+            issue_grad(it, false, 1);
+            mma_commit_lead(lead, bar(C::bOE + it % kOS));  // dO stage free once dV has read it
             if (more) {
-                if (!(ok = mbar_wait(bar(C::bF + (s ^ 1)), ((it + 1) >> 1) & 1, abort_flag, p.err,
-                                     BSATTN_FLAG_TIMEOUT)))
-                    break;
-                tc_fence_after();
-                issue_s(s ^ 1, 0);
+                if (!(ok = wait(C::bDL, it))) break;
+                if (!(ok = wait(C::bQF + (it + 1) % kQS, (it + 1) / kQS))) break;
+                issue_mm(it + 1, false);
+                mma_commit_lead(lead, bar(C::bS));
             }
-            if (!(ok = mbar_wait(bar(C::bPR2), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))) break;
-            tc_fence_after();
-            issue_grad(s, 1, it);
-            mma_commit_lead(lead, bar(C::bE + s));  // stage free once these have read it
-            if (more) issue_s(s ^ 1, 1);
+            if (!(ok = wait(C::bDS, it))) break;
+            issue_grad(it, true, 0);
+            if (!(ok = wait(C::bDS + 1, it))) break;
+            issue_grad(it, true, 1);
+            mma_commit_lead(lead, bar(C::bQE + it % kQS));  // Q stage and its vectors free
+            if (more) {
+                if (!(ok = wait(C::bOF + (it + 1) % kOS, (it + 1) / kOS))) break;
+                issue_mm(it + 1, true);
+                mma_commit_lead(lead, bar(C::bP));
+            }
         }
         if (ok) mma_commit_lead(lead, bar(C::bDone));
         mma_commit_lead(lead, bar(C::bDrain));
@@ -677,12 +707,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float *vecs = reinterpret_cast<const float *>(gbase + C::kVec);
         bool ok = true;
         for (int it = 0; it < total; ++it) {
-            const int s = it & 1;
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bF + s), (it >> 1) & 1, abort_flag, p.err,
+            const int qs = it % kQS;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::bQF + qs), (it / kQS) & 1, abort_flag, p.err,
                                                          BSATTN_FLAG_TIMEOUT))))
                 break;
-            const int m = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 0];
-            const bool msk = reinterpret_cast<volatile int32_t *>(info)[s * 4 + 1] != 0;
+            if (!(ok = __all_sync(0xffffffffu,
+                                  mbar_wait(bar(C::bS), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))))
+                break;
+            tc_fence_after();
+            const int m = reinterpret_cast<volatile int32_t *>(info)[qs * 2 + 0];
+            const bool msk = reinterpret_cast<volatile int32_t *>(info)[qs * 2 + 1] != 0;
             // kept query columns of this key row: [lo, hi) (query i = m * 128 + column)
             long long lo = 0, hi = kTile;
             const bool row_on = r < (msk ? klim_mask : klim_full);
@@ -701,20 +735,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             const bool doc = msk && row_on && p.kind == BSATTN_MASK_DOCUMENT;
             const int32_t dk = doc ? p.doc_k[sg.k0 + j] : 0;
-            const float *nl2 = vecs + s * 256, *ndd = nl2 + 128;  // -LSE2, -D of the stage's queries
+            const float *nl2 = vecs + qs * 256, *ndd = nl2 + 128;  // -LSE2, -D of the stage's queries
+            const uint32_t tS = region(it) + la, tP = region(it + 1) + la;
+            // P = 2^(s log2(e) scale - LSE2), two columns per packed instruction;
+            // dropped columns enter the exponential as -inf.  A chunk every lane
+            // keeps whole takes the form without selects.
+            float pr[2][32];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(half ? C::bSR2 : C::bSR), it & 1, abort_flag,
-                                                             p.err, BSATTN_FLAG_TIMEOUT))))
-                    break;
-                tc_fence_after();
-                const int c = 2 * half + cg;  // query chunk: columns [32 c, 32 c + 32)
-                uint32_t vs[32], vp[32];
-                tmem_ld32(tS + la + 32u * c, vs);
-                tmem_ld32(tP + la + 32u * c, vp);
+            for (int k = 0; k < 2; ++k) {
+                const int c = cg + 2 * k;  // query chunk: columns [32 c, 32 c + 32)
+                uint32_t vs[32];
+                tmem_ld32(tS + 32u * c, vs);
                 tmem_wait_ld();
                 reg_fence(vs);
-                reg_fence(vp);
                 uint32_t keep = bwd_span_bits(lo - 32 * c, hi - 32 * c);
                 if (doc) {
                     keep = 0u;
@@ -724,40 +757,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             keep |= 1u << x;
                     }
                 }
-                uint32_t pw[16], dw[16];
-                // P = 2^(s log2(e) scale - LSE2), dS = P (dP - D), two columns per
-                // packed instruction; dropped columns enter the exponential as -inf.
-                // A chunk every lane keeps whole takes the form without selects.
+                uint32_t pw[16];
                 auto form = [&](auto masked) {
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
-                        const int c0 = 32 * c + 2 * x;
-                        const float2 nl = *reinterpret_cast<const float2 *>(nl2 + c0);
-                        const float2 nd = *reinterpret_cast<const float2 *>(ndd + c0);
-                        float x0, x1, t0, t1, d0, d1;
+                        const float2 nl = *reinterpret_cast<const float2 *>(nl2 + 32 * c + 2 * x);
+                        float x0, x1;
                         ffma2(x0, x1, __uint_as_float(vs[2 * x]), __uint_as_float(vs[2 * x + 1]), sl2, sl2,
                               nl.x, nl.y);
                         if constexpr (decltype(masked)::value) {
                             x0 = ((keep >> (2 * x)) & 1u) ? x0 : -INFINITY;
                             x1 = ((keep >> (2 * x + 1)) & 1u) ? x1 : -INFINITY;
                         }
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        fadd2(t0, t1, __uint_as_float(vp[2 * x]), __uint_as_float(vp[2 * x + 1]), nd.x, nd.y);
-                        fmul2(d0, d1, p0, p1, t0, t1);
-                        pw[x] = pack_bf16x2(p0, p1);
-                        dw[x] = pack_bf16x2(d0, d1);
+                        pr[k][2 * x] = ex2_approx(x0);
+                        pr[k][2 * x + 1] = ex2_approx(x1);
+                        pw[x] = pack_bf16x2(pr[k][2 * x], pr[k][2 * x + 1]);
                     }
                 };
                 if (__all_sync(0xffffffffu, keep == 0xffffffffu)) form(std::false_type{});
                 else form(std::true_type{});
-                tmem_st16(tS + la + 32u * c, pw);
-                tmem_st16(tP + la + 32u * c, dw);
+                tmem_st16(tS + 32u * c, pw);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(half ? C::bPR2 : C::bPR));
+                if (lane == 0) mbar_arrive(bar(C::bPt + k));
             }
-            if (!ok) break;
+            // dS = P (dP - D): dP^T of this tile into registers, its region
+            // released, then dS^T of each chunk
+            if (!(ok = __all_sync(0xffffffffu,
+                                  mbar_wait(bar(C::bP), it & 1, abort_flag, p.err, BSATTN_FLAG_TIMEOUT))))
+                break;
+            tc_fence_after();
+            uint32_t vp[2][32];
+            tmem_ld32(tP + 32u * cg, vp[0]);
+            tmem_ld32(tP + 32u * (cg + 2), vp[1]);
+            tmem_wait_ld();
+            reg_fence(vp[0]);
+            reg_fence(vp[1]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::bDL));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = cg + 2 * k;
+                uint32_t dw[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float2 nd = *reinterpret_cast<const float2 *>(ndd + 32 * c + 2 * x);
+                    float t0, t1, d0, d1;
+                    fadd2(t0, t1, __uint_as_float(vp[k][2 * x]), __uint_as_float(vp[k][2 * x + 1]), nd.x, nd.y);
+                    fmul2(d0, d1, pr[k][2 * x], pr[k][2 * x + 1], t0, t1);
+                    dw[x] = pack_bf16x2(d0, d1);
+                }
+                tmem_st16(tS + 32u * c + 16u, dw);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::bDS + k));
+            }
         }
         // ------------------------------------------------- epilogue --
         if (ok && total > 0) {
