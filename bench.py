@@ -387,7 +387,7 @@ def time_bwd(wl, dw, meta, out, lse, err, stream, flop_fwd, iters=5):
     mean = statistics.mean(ms)
     flop = 2.5 * flop_fwd
     return {"ms": mean, "tflops": flop / (mean * 1e-3) / 1e12, "flop": flop,
-            "launches_per_call": 4, "grad_dtype": "bf16",
+            "launches_per_call": 6 + (1 if wl.varlen else 0), "grad_dtype": "bf16",
             "note": "flop = 2.5 x forward flop over computed blocks; events around each call"}
 
 
@@ -792,7 +792,9 @@ def run_native(args):
                 "pipeline": "copy-in, compute and copy-out on three streams, two buffer sets"},
         "meta_formats": meta_formats,
         "proxy_ab": proxy_ab,
-        "bwd": bwd if bwd is None or "ms" not in bwd else dict(bwd, frac=bwd["tflops"] / peak),
+        "bwd": bwd if bwd is None or "ms" not in bwd else dict(
+            bwd, frac=bwd["tflops"] / peak,
+            frac_of_sustained=bwd["tflops"] / float(peaks.get("bf16_tflops_sustained", peak))),
         "per_config": cfg_lines,
         "sparse_blocks": blocks_ab,
         "gpu_launches": K * (2 + (1 if wl.varlen else 0) + (1 if sched_ws is not None else 0)),
