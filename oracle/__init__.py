@@ -11,9 +11,9 @@ Functions follow the varlen block-sparsity pull request (flash-attention
 learning note ("Dense FlashAttention vs Block-Sparse Attention", section 2) for
 the reversed, -1-padded index lists; the C file's header lists each source and
 every reading taken where the pages leave a step open.  The backward (numpy,
-fp64: ``bwd_f64`` and its per-tile forms) differentiates the same definition;
+fp64: ``bwd_f64`` and its per-tile and per-head forms) differentiates the same definition;
 it is pinned by central finite differences and fp64 torch autograd, and the
-per-tile forms by the dense one (tests/test_oracle_bwd.py).
+per-tile and per-head forms by the dense one (tests/test_oracle_bwd.py).
 """
 from __future__ import annotations
 
@@ -572,6 +572,25 @@ def bwd_dq_tile(wl, q, k, v, dout, meta, b, h, m):
     batched layout, `meta` the oracle's own lists."""
     _, _, keys, _, dS, _, kf, _ = _tile_grads(wl, q, k, v, dout, meta, b, h, m)
     return wl.scale * (dS @ kf) if keys.size else np.zeros((dS.shape[0], q.shape[3]))
+
+
+def bwd_head(wl, q, k, v, dout, meta, b, h):
+    """(dQ, dK, dV) (fp64 [S_q, D], [S_k, D], [S_k, D]) of head h of sequence b:
+    bwd_f64's definition evaluated one Q tile at a time.  Each Q tile's rows
+    give their dQ rows directly and add P^T dO and scale dS^T Q into the dV and
+    dK rows of the keys its lists name, so a head of a long sequence needs no
+    dense [S_q, S_k] matrix."""
+    Sq, Sk = int(wl.seqlens_q[b]), int(wl.seqlens_k[b])
+    D = q.shape[3]
+    dq, dk, dv = np.zeros((Sq, D)), np.zeros((Sk, D)), np.zeros((Sk, D))
+    for m in range(-(-Sq // wl.tile_m)):
+        r0, r1, keys, P, dS, qf, kf, g = _tile_grads(wl, q, k, v, dout, meta, b, h, m)
+        if not keys.size:
+            continue
+        dq[r0:r1] = wl.scale * (dS @ kf)
+        dv[keys] += P.T @ g
+        dk[keys] += wl.scale * (dS.T @ qf)
+    return dq, dk, dv
 
 
 def bwd_dkdv_tile(wl, q, k, v, dout, meta, b, h, n):

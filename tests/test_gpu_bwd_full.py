@@ -1,12 +1,14 @@
 """Backward at the benchmark workloads' full sizes, in the launch configuration
 bench.py times (bf16 forward output, bf16 gradients), against the oracle.
 
-The batched random workload (B 2, H 4, S 1024) is compared element by element
-with the dense fp64 backward; the varlen workload (8 sequences of 100-4096
-tokens, H 16), the VSA (H 24, S 61440) and the long-context (H 32, S 131072)
-workloads on sampled Q tiles (dQ rows) and KV tiles (dK, dV rows), each
-computed by the oracle's per-tile backward (per sequence for varlen).  Tolerance as in
-test_gpu_bwd.py, per sampled tensor: max |G - G_ref| <= 2e-2 max |G_ref| and
+The batched random workload (B 2, H 4, S 1024) and the varlen workload (8
+sequences of 100-4096 tokens, H 16) are compared element by element with the
+dense fp64 backward (per sequence for varlen).  The VSA (H 24, S 61440) and
+long-context (H 32, S 131072) workloads are compared on every row of their
+first and last heads (dQ, dK, dV of the whole head, by the oracle's per-head
+backward, which walks the head's Q tiles) and on sampled Q tiles (dQ rows) and
+KV tiles (dK, dV rows) of random heads.  Tolerance as in test_gpu_bwd.py, per
+compared tensor: max |G - G_ref| <= 2e-2 max |G_ref| and
 ||G - G_ref||_F <= 1e-2 ||G_ref||_F."""
 import numpy as np
 import pytest
@@ -57,7 +59,7 @@ def test_bwd_batched_random_workload_elementwise():
 
 
 @pytest.mark.parametrize("cfg", [4, 5])
-def test_bwd_full_size_sampled(cfg):
+def test_bwd_full_size_whole_heads_and_sampled_tiles(cfg):
     wl = make_workload(cfg)
     (q, k, v, g), (dq, dk, dv) = _run(wl)
     assert all(np.all(np.isfinite(t)) for t in (dq, dk, dv))
@@ -80,25 +82,17 @@ def test_bwd_full_size_sampled(cfg):
         c0 = n * wl.tile_n
         _close(dk[b, c0:c0 + rk.shape[0], h], rk, f"dk h={h} n={n}")
         _close(dv[b, c0:c0 + rv.shape[0], h], rv, f"dv h={h} n={n}")
+    # whole heads: the first and the last, every row of dQ, dK and dV
+    for h in (0, wl.H - 1):
+        hq, hk, hv = oracle.bwd_head(wl, q, k, v, g, meta, b, h)
+        _close(dq[b, :, h], hq, f"dq head {h}")
+        _close(dk[b, :, h], hk, f"dk head {h}")
+        _close(dv[b, :, h], hv, f"dv head {h}")
 
 
-def test_bwd_varlen_workload_sampled():
+def test_bwd_varlen_workload_elementwise():
     wl = make_workload(3)
     (q, k, v, g), (dq, dk, dv) = _run(wl)
-    assert all(np.all(np.isfinite(t)) for t in (dq, dk, dv))
-    meta = oracle.build_meta(wl)
-    rng = np.random.default_rng(703)
-    picks = [int(rng.integers(wl.B)) for _ in range(4)] + [wl.B - 1]
-    for j, b in enumerate(picks):
-        view, mb, qs, ks = oracle.seq_view(wl, meta, b)
-        qb, kb, vb, gb = q[qs][None], k[ks][None], v[ks][None], g[qs][None]
-        h = int(rng.integers(wl.H))
-        m = view.num_m - 1 if j == len(picks) - 1 else int(rng.integers(view.num_m))
-        n = view.num_n - 1 if j == len(picks) - 1 else int(rng.integers(view.num_n))
-        ref = oracle.bwd_dq_tile(view, qb, kb, vb, gb, mb, 0, h, m)
-        r0 = qs.start + m * wl.tile_m
-        _close(dq[r0:r0 + ref.shape[0], h], ref, f"dq b={b} h={h} m={m}")
-        rk, rv = oracle.bwd_dkdv_tile(view, qb, kb, vb, gb, mb, 0, h, n)
-        c0 = ks.start + n * wl.tile_n
-        _close(dk[c0:c0 + rk.shape[0], h], rk, f"dk b={b} h={h} n={n}")
-        _close(dv[c0:c0 + rv.shape[0], h], rv, f"dv b={b} h={h} n={n}")
+    ref = oracle.bwd(wl, q, k, v, oracle.build_meta(wl), g)
+    for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        _close(got, r, name)

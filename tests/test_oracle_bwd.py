@@ -103,6 +103,22 @@ def test_per_tile_backward_equals_the_dense_one(c):
                 assert np.max(np.abs(tv - dv[b, c0:c0 + tv.shape[0], h]), initial=0) < 1e-12
 
 
+@pytest.mark.parametrize("c", CASES)
+def test_per_head_backward_equals_the_dense_one(c):
+    # the whole-head form (Q tile by Q tile, for full-size checks) against bwd_f64
+    wl = random_workload(**c)
+    q, k, v = wl.qkv()
+    g = wl.tensor("do")
+    meta = oracle.build_meta(wl)
+    dq, dk, dv = oracle.bwd(wl, q, k, v, meta, g)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            hq, hk, hv = oracle.bwd_head(wl, q, k, v, g, meta, b, h)
+            for got, ref in ((hq, dq[b, :, h]), (hk, dk[b, :, h]), (hv, dv[b, :, h])):
+                assert got.shape == ref.shape
+                assert np.max(np.abs(got - ref), initial=0) < 1e-12
+
+
 VARLEN_CASES = [
     dict(seed=211, B=3, H=2, D=8, seqlens_q=[300, 129, 200], seqlens_k=[260, 400, 128],
          varlen=True, kind=MASK_CAUSAL),
