@@ -16,10 +16,11 @@
 //   3. a row pass writing -D and -LSE * log2(e) into rows padded to 128 per Q
 //      tile (negated, so that the gradient kernels add them);
 //   4. the dK / dV kernel: one CTA per KV tile, S^T = K Q^T and dP^T = V dO^T per
-//      listed Q tile on tcgen05 in two query halves, P^T and dS^T formed per key
-//      row in TMEM, dV += P^T dO and dK += dS^T Q accumulated in TMEM; half h of
-//      the next Q tile is issued as soon as this one's half h is done, so the
-//      products of one half overlap the elementwise work of the other;
+//      listed Q tile on tcgen05 as full-width products in two alternating TMEM
+//      regions, P^T and dS^T formed per key row into the S^T region, dV += P^T dO
+//      and dK += dS^T Q accumulated in TMEM; the next Q tile's S^T goes into the
+//      dP^T region as soon as dP^T is in registers, so each product overlaps the
+//      elementwise step the next one waits for;
 //   5. the dQ kernel: one CTA per Q tile, S = Q K^T and dP = dO V^T per listed KV
 //      tile as full-width products, dS per query row into one of two TMEM
 //      buffers, dQ += dS K accumulated in TMEM; the next KV tile's S and dP are
