@@ -370,6 +370,44 @@ def fwd_proxy(wl, q, k, v, k_sum, v_sum, sel_map):
     return out, lse
 
 
+def fwd_proxy_rows(wl, q, k, v, k_sum, v_sum, sel_map, tok, head, batch=None):
+    """fwd_proxy's definition for selected rows only: row tok[r] of head head[r]
+    (of sequence batch[r], default 0).  Rows are grouped by their Q tile, whose
+    selected tiles' keys enter exactly and whose other tiles enter as the
+    weighted summaries, so a long sequence needs no [S_q, S_k] matrix.  Returns
+    O [R, D] and LSE [R] (natural log), fp64."""
+    ks = _widen(k_sum) if np.asarray(k_sum).dtype == np.uint16 else np.asarray(k_sum, np.float64)
+    vs = _widen(v_sum) if np.asarray(v_sum).dtype == np.uint16 else np.asarray(v_sum, np.float64)
+    tok = np.asarray(tok, np.int64)
+    head = np.asarray(head, np.int64)
+    batch = np.zeros_like(tok) if batch is None else np.asarray(batch, np.int64)
+    Sk = k.shape[1]
+    D = q.shape[3]
+    tm, tn = wl.tile_m, wl.tile_n
+    nn = -(-Sk // tn)
+    w = np.array([min(tn, Sk - n * tn) for n in range(nn)], np.float64)
+    out = np.zeros((tok.size, D))
+    lse = np.zeros(tok.size)
+    groups = {}
+    for r in range(tok.size):
+        groups.setdefault((int(batch[r]), int(head[r]), int(tok[r]) // tm), []).append(r)
+    for (b, h, m), rows in groups.items():
+        rows = np.asarray(rows)
+        sel = np.asarray(sel_map[b, h, m], dtype=bool)               # [nn]
+        keys = np.concatenate([np.arange(n * tn, min((n + 1) * tn, Sk)) for n in np.flatnonzero(sel)]
+                              ) if sel.any() else np.zeros(0, np.int64)
+        qf = _widen(q[b, tok[rows], h])                              # [R, D]
+        s = wl.scale * qf @ _widen(k[b, keys, h]).T                  # exact keys
+        t = wl.scale * qf @ ks[b, ~sel, h].T                         # summaries of the others
+        mx = np.maximum(s.max(axis=1, initial=-np.inf), t.max(axis=1, initial=-np.inf))[:, None]
+        es, et = np.exp(s - mx), np.exp(t - mx)
+        den = es.sum(axis=1) + (et * w[~sel][None]).sum(axis=1)
+        num = es @ _widen(v[b, keys, h]) + et @ vs[b, ~sel, h]
+        out[rows] = num / den[:, None]
+        lse[rows] = mx[:, 0] + np.log(den)
+    return out, lse
+
+
 # ---- backward (the gradients of the forward defined above; batched) ---------
 
 def allowed_mask(wl, meta, b, h):

@@ -2,7 +2,11 @@
 block-sparse attention", FlashInfer #4872) and the KV summaries against the
 oracle: O within 5e-3 and LSE within 1e-3 of the fp64 definition fed the same
 bf16 summaries; summaries within one bf16 ulp of the fp64 mean / sum; with every
-tile selected the proxy forward equals the exact forward bit for bit."""
+tile selected the proxy forward equals the exact forward bit for bit.  At full
+size, on the video sparse attention map (B 1, H 24, S 61440, mask kind none, as
+bench.py's proxy A/B runs it), every row of the last head and 400 random rows
+are compared with the oracle's per-row form, and the bf16 output is RNE of the
+fp32 one everywhere."""
 import math
 
 import numpy as np
@@ -97,3 +101,37 @@ def test_proxy_with_every_tile_selected_equals_exact_forward():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(out, out_e) and torch.equal(lse, lse_e)
+
+
+def test_proxy_forward_full_size_on_the_benchmark_map():
+    from workloads import make_workload
+    from workloads.device import DeviceWorkload as DW
+    wl = make_workload(4)
+    q, k, v = wl.qkv()
+    dw = DW(wl, "cuda", qkv=(q, k, v))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sq, sk = dw.seqlens()
+    meta = dw.alloc_meta()
+    stream = torch.cuda.current_stream().cuda_stream
+    st = bsa.bsattn_build_meta(dw.block_map, None, None, sq, sk, None, bsa.MASK_NONE, None, meta, err, stream)
+    assert st == bsa.BSATTN_OK, bsa.status_string(st)
+    nn = math.ceil(sk / 128)
+    ks = torch.empty((wl.B, nn, wl.H, wl.D), dtype=torch.bfloat16, device="cuda")
+    vs = torch.empty_like(ks)
+    st = bsa.bsattn_kv_summaries(dw.k, dw.v, wl.B, sk, wl.H, wl.D, ks, vs, stream)
+    assert st == bsa.BSATTN_OK, bsa.status_string(st)
+    words, W = to_bitmask(wl, wl.block_map)
+    d_words = torch.from_numpy(words.view(np.int32)).to("cuda")
+    out, lse = _proxy(wl, dw, err, meta, ks, vs, d_words, W)
+    out16, _ = _proxy(wl, dw, err, meta, ks, vs, d_words, W, out_dtype=torch.bfloat16)
+    assert int(err.item()) == 0
+    assert torch.equal(out16.view(torch.int16), out.to(torch.bfloat16).view(torch.int16))
+    o = out.cpu().numpy()[0]            # [S, H, D]
+    l = lse.cpu().numpy()[0]            # [H, S]
+    rng = np.random.default_rng(404)
+    tok = np.concatenate([np.arange(sq), rng.integers(0, sq, 400)])
+    head = np.concatenate([np.full(sq, wl.H - 1), rng.integers(0, wl.H, 400)])
+    o_ref, l_ref = oracle.fwd_proxy_rows(wl, q, k, v, _bits(ks), _bits(vs), wl.block_map, tok, head)
+    e_o = float(np.max(np.abs(o[tok, head].astype(np.float64) - o_ref)))
+    e_l = float(np.max(np.abs(l[head, tok].astype(np.float64) - l_ref)))
+    assert e_o <= 5e-3 and e_l <= 1e-3, (e_o, e_l)

@@ -3,8 +3,10 @@ support proxy-compensated block-sparse attention", FlashInfer #4872), pinned to
 closed forms: a tile whose keys are all equal is represented exactly by its
 summaries, so proxies over such tiles reproduce exact attention (computed by the
 C oracle); with every tile selected the proxy form is exact attention; and a
-hand-worked mean / sum over a partial tile."""
+hand-worked mean / sum over a partial tile.  The per-row form (for full-size
+checks) equals the dense one on every row."""
 import numpy as np
+import pytest
 
 import oracle
 from workloads.configs import MASK_NONE, random_workload
@@ -73,3 +75,18 @@ def test_mixed_selection_splits_between_exact_and_proxy():
     wl.block_map = np.ones_like(wl.block_map)
     o_e, l_e = oracle.fwd(wl, q, k, v, oracle.build_meta(wl))
     assert np.max(np.abs(o_p - o_e)) < 1e-12 and np.max(np.abs(l_p - l_e)) < 1e-12
+
+
+@pytest.mark.parametrize("seed,density,sk", [(701, 0.5, 300), (702, 0.0, 640), (703, 0.3, 1000)])
+def test_proxy_rows_equal_the_dense_proxy(seed, density, sk):
+    # the per-row form (grouped by Q tile, for full-size checks) against fwd_proxy on every row
+    wl = random_workload(seed, B=2, H=2, D=16, seqlens_q=[384, 384], seqlens_k=[sk, sk],
+                         kind=MASK_NONE, density=density, force_diag=density > 0)
+    q, k, v = wl.qkv()
+    km, vsum = oracle.kv_summaries(wl, k, v)
+    o_ref, l_ref = oracle.fwd_proxy(wl, q, k, v, km, vsum, wl.block_map)
+    S, H = 384, 2
+    b, t, h = np.meshgrid(np.arange(2), np.arange(S), np.arange(H), indexing="ij")
+    o, l = oracle.fwd_proxy_rows(wl, q, k, v, km, vsum, wl.block_map, t.ravel(), h.ravel(), b.ravel())
+    assert np.max(np.abs(o - o_ref[b.ravel(), t.ravel(), h.ravel()])) < 1e-12
+    assert np.max(np.abs(l - l_ref[b.ravel(), h.ravel(), t.ravel()])) < 1e-12
